@@ -1,0 +1,102 @@
+// Internal definitions shared by the host layer (mac_api.cu) and the kernels
+// (mac_kernels.cu) of the MAC-Attention decode-step library.  Not part of the
+// public ABI (include/mac.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace macgpu {
+
+constexpr int kD = 128;                 // head_dim
+constexpr int kPage = 16;               // tokens per KV page / per staged block
+constexpr int kMaxRing = 64;            // ring entries per (request, head)
+constexpr int kMaxGroup = 32;           // query heads per KV head
+constexpr int kMaxCtas = 1024;          // upper bound of the attention grid
+constexpr int kMaxGroupsPerStep = 8192; // max_batch * kv_heads
+constexpr int kAttnWarps = 4;           // warps per attention CTA
+constexpr int kAttnStages = 3;          // pipeline stages per page lane
+constexpr int kStageBytes = 2 * kPage * kD * 2;   // one K page + one V page (bf16): 8 KB
+constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
+constexpr int kMinChunk = 64;           // smallest work-item span in tokens
+
+// device error bits
+enum : uint32_t { kErrPage = 1u, kErrSlot = 2u, kErrPos = 4u };
+
+// device counters
+enum { kStSteps = 0, kStDecisions, kStHits, kStKvRead, kStKvFull, kStDirect, kStItems, kStCount };
+
+// Device-side view of one handle: dimensions and carved buffer pointers.
+struct Layout {
+    int H, Hkv, G, ring_len, band_r;
+    int max_batch;
+    int paged;
+    int pages_per_req;        // page-table row length (paged) / blocks per request (contiguous)
+    int num_pages;            // paged: pool pages
+    int ctx_stride;           // contiguous: tokens reserved per (request, kv-head)
+    int item_cap;
+    float tau2;               // tau^2 (fp32)
+    float scale_log2;         // sm_scale * log2(e)
+
+    __nv_bfloat16 *k_pool, *v_pool;
+    int32_t *page_table;      // [max_batch][pages_per_req]
+
+    // rings
+    int32_t *ring_pos;        // [max_batch][L] 1-based position, 0 = empty
+    __nv_bfloat16 *ring_q;    // [max_batch][H][L][D]
+    float *ring_o;            // [max_batch][H][L][D]
+    float *ring_lse;          // [max_batch][H][L]
+
+    // per-request state
+    int32_t *kv_len;          // [max_batch]
+    int32_t *step_ctr;        // [max_batch]
+    int32_t *m_cur;           // [max_batch] position m of the step in flight
+    int32_t *slot_cur;        // [max_batch] ring slot the step in flight inserts into
+
+    // decisions [max_batch * H]
+    int32_t *dec_own_slot, *dec_own_hit, *dec_slot, *dec_lo;
+    float *dec_D, *dec_qn2;
+    int32_t *forced_slot;
+    __nv_bfloat16 *q_stash;   // [max_batch][H][D] post-RoPE query kept for Amend
+
+    // plan
+    int32_t *grp_lo;          // [max_batch * Hkv]
+    int32_t *grp_item_off;    // [max_batch * Hkv + 1]
+    int4 *items;              // [item_cap] {b*Hkv+g, lo, hi, segment}
+    int32_t *n_items;
+    uint32_t *ticket;
+
+    // partial summaries of work items: unnormalised o, (max, sum) in log2 units
+    float *part_o;            // [item_cap][G][D]
+    float2 *part_ml;          // [item_cap][G]
+
+    // merged summaries kept for Amend
+    float *as_full_o, *as_full_lse;   // AS_{1:m}
+    float *as_pre_o, *as_pre_lse;     // AS_{1:m-r} formed directly (fallback of the removal)
+
+    unsigned long long *stats;        // [kStCount]
+    uint32_t *err;
+};
+
+struct StepArgs {
+    int batch;
+    const __nv_bfloat16 *q_pre, *q_post, *k_new, *v_new;
+    __nv_bfloat16 *out;
+    float *lse_out;
+    int force;        // use forced_slot instead of the Match decision
+    int full_mode;    // full attention, no Match / Amend
+    int grid_ctas;    // attention CTAs
+    int plan_mode;    // 0 balanced, 1 equal split per group
+};
+
+// launchers (mac_kernels.cu)
+cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s);
+cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_append(const Layout &L, int req, int start, int n, const __nv_bfloat16 *k,
+                          const __nv_bfloat16 *v, cudaStream_t s);
+cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm);
+
+}  // namespace macgpu

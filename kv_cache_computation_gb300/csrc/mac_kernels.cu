@@ -1,0 +1,851 @@
+// sm_103a kernels of the MAC-Attention decode step.
+//
+// One decode step is four launches:
+//   match_plan  (critical path) KV append of the new token; Match of each
+//               query head's pre-RoPE query against its ring (Figure 2(a) of
+//               the MAC-Attention paper); per-head band+tail spans; and, in
+//               the last block, the span-proportional work list (Figure 3(b),
+//               "load-balanced planning").
+//   attention   (critical path) persistent split-KV attention over the work
+//               list: each item streams 16-token KV pages of one KV head
+//               through a cp.async shared-memory pipeline and evaluates all
+//               query heads of the group with bf16 tensor-core tiles,
+//               keeping fp32 online-softmax partials (Figure 2(b), Complete).
+//   combine     (critical path) log-domain merge of the partials and, on a
+//               hit, of the reused AS_{1:p-r} from the ring (Figure 2(b)).
+//   amend       (side stream) recompute AS_{m-r+1:m}, log-domain removal to
+//               AS_{1:m-r}, ring insert (Figure 2(c)).
+//
+// Conventions: token index j (0-based) is the paper's position j+1; ranges
+// [lo, hi) are half-open over indices.  Scores are kept in log2 units
+// (scaled by sm_scale * log2 e) inside the kernels; summaries that leave the
+// kernels (ring, lse_out) use natural-log units.
+#include "mac_internal.cuh"
+
+#include <math_constants.h>
+
+namespace macgpu {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16 *p)
+{
+    uint2 u = *reinterpret_cast<const uint2 *>(p);
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&u.x);
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&u.y);
+    float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+// Element offset of the 16-token block `pg` of (request b, kv-head g).  Both
+// layouts keep the block's 16 x 128 bf16 keys (and values) contiguous (4 KB).
+__device__ __forceinline__ size_t kv_block(const Layout &L, int b, int g, int pg, bool &ok)
+{
+    if (pg < 0 || pg >= L.pages_per_req) {
+        ok = false;
+        return 0;
+    }
+    if (L.paged) {
+        int phys = L.page_table[(size_t)b * L.pages_per_req + pg];
+        if ((unsigned)phys >= (unsigned)L.num_pages) {
+            ok = false;
+            return 0;
+        }
+        return ((size_t)phys * L.Hkv + g) * (kPage * kD);
+    }
+    return (((size_t)b * L.Hkv + g) * L.ctx_stride + (size_t)pg * kPage) * kD;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void named_bar(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t &a0, uint32_t &a1, uint32_t &a2, uint32_t &a3, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t &a0, uint32_t &a1, uint32_t &a2, uint32_t &a3, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v)
+{
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// log(1 - e^x), x <= 0: Maechler (2012), "Accurately computing
+// log(1 - exp(-|a|))" -- log(-expm1(x)) above -ln 2, log1p(-exp(x)) below.
+__device__ __forceinline__ float log1mexp_f(float x)
+{
+    return x > -kLn2 ? logf(-expm1f(x)) : log1pf(-expf(x));
+}
+
+// number of chunks of [a, b) when cut at multiples of C
+__device__ __forceinline__ int n_chunks(int a, int b, int C)
+{
+    return b > a ? (b - 1) / C - a / C + 1 : 0;
+}
+
+__device__ __forceinline__ int round_up16(long long x)
+{
+    return (int)((x + 15) / 16 * 16);
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim a multiple of 32,
+// up to 1024).  Returns the exclusive prefix; *total gets the sum.
+__device__ int block_exclusive_scan(int v, int *total)
+{
+    __shared__ int warp_tot[32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) warp_tot[lane] = t;   // inclusive warp prefix
+    }
+    __syncthreads();
+    int before = (w > 0 ? warp_tot[w - 1] : 0) + x - v;
+    *total = warp_tot[nw - 1];
+    __syncthreads();
+    return before;
+}
+
+__device__ __forceinline__ int group_chunk(const StepArgs &a, int s_C, int splits, int lo, int hi, int scale)
+{
+    int C = a.plan_mode == 0 ? s_C : max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
+    return C * scale;
+}
+
+// ---------------------------------------------------------------------------
+// Planning (last block of match_plan).  Per (request, kv-head) group, the
+// streamed span is [lo_g, m) with lo_g the smallest band+tail start of the
+// group's heads; Amend's band [m-r, m) is cut off as its own segment so the
+// direct form of AS_{1:m-r} is available to Amend.  Chunks are cut at
+// multiples of C (a multiple of 16: page aligned).  Balanced mode picks C so
+// the whole step splits into about one item per attention CTA -- longer
+// spans get proportionally more CTAs (Figure 3(b)); equal mode gives every
+// group the same number of items whatever its span (unbalanced baseline).
+// ---------------------------------------------------------------------------
+__device__ void plan_work(const Layout &L, const StepArgs &a)
+{
+    const int nbg = a.batch * L.Hkv;
+    const int nthr = blockDim.x;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    long long T = 0, Tfull = 0;
+    for (int bg = threadIdx.x; bg < nbg; bg += nthr) {
+        int b = bg / L.Hkv;
+        int hi = __ldcg(&L.kv_len[b]) + 1;
+        int lo = __ldcg(&L.grp_lo[bg]);
+        T += hi - lo;
+        Tfull += hi;
+    }
+    __shared__ long long red_t[32], red_f[32];
+    __shared__ int s_C;
+    for (int o = 16; o; o >>= 1) {
+        T += __shfl_xor_sync(0xffffffffu, T, o);
+        Tfull += __shfl_xor_sync(0xffffffffu, Tfull, o);
+    }
+    if (lane == 0) {
+        red_t[w] = T;
+        red_f[w] = Tfull;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long st = 0, sf = 0;
+        for (int i = 0; i < (nthr >> 5); i++) {
+            st += red_t[i];
+            sf += red_f[i];
+        }
+        T = st;
+        Tfull = sf;
+        int C = round_up16((T + a.grid_ctas - 1) / a.grid_ctas);
+        s_C = C < kMinChunk ? kMinChunk : C;
+    }
+    __syncthreads();
+    const int sC = s_C;
+    const int splits = a.grid_ctas / nbg > 1 ? a.grid_ctas / nbg : 1;
+    int scale = 1;
+    // counts, growing C until the list fits the partial buffers
+    for (int iter = 0; iter < 40; iter++) {
+        int cnt = 0;
+        for (int bg = threadIdx.x; bg < nbg; bg += nthr) {
+            int b = bg / L.Hkv;
+            int hi = __ldcg(&L.kv_len[b]) + 1;
+            int lo = __ldcg(&L.grp_lo[bg]);
+            int split = a.full_mode ? lo : max(lo, hi - L.band_r);
+            int C = group_chunk(a, sC, splits, lo, hi, scale);
+            cnt += n_chunks(lo, split, C) + n_chunks(split, hi, C);
+        }
+        int tot;
+        block_exclusive_scan(cnt, &tot);
+        if (tot <= L.item_cap) break;
+        scale *= 2;
+    }
+    // offsets and items; groups are taken in rounds so the list stays in order
+    int base = 0;
+    for (int r0 = 0; r0 < nbg; r0 += nthr) {
+        const int bg = r0 + threadIdx.x;
+        int cnt = 0, lo = 0, hi = 0, split = 0, C = kMinChunk;
+        if (bg < nbg) {
+            int b = bg / L.Hkv;
+            hi = __ldcg(&L.kv_len[b]) + 1;
+            lo = __ldcg(&L.grp_lo[bg]);
+            split = a.full_mode ? lo : max(lo, hi - L.band_r);
+            C = group_chunk(a, sC, splits, lo, hi, scale);
+            cnt = n_chunks(lo, split, C) + n_chunks(split, hi, C);
+        }
+        int tot;
+        const int off = base + block_exclusive_scan(cnt, &tot);
+        if (bg < nbg) {
+            L.grp_item_off[bg] = off;
+            int k = off;
+            for (int seg = 0; seg < 2; seg++) {
+                const int s0 = seg == 0 ? lo : split, s1 = seg == 0 ? split : hi;
+                if (s1 <= s0) continue;
+                for (int c = s0 / C; c <= (s1 - 1) / C; c++)
+                    L.items[k++] = make_int4(bg, max(s0, c * C), min(s1, (c + 1) * C), seg);
+            }
+        }
+        base += tot;
+    }
+    if (threadIdx.x == 0) {
+        L.grp_item_off[nbg] = base;
+        *L.n_items = base;
+        atomicAdd(&L.stats[kStSteps], 1ull);
+        atomicAdd(&L.stats[kStKvRead], (unsigned long long)T);
+        atomicAdd(&L.stats[kStKvFull], (unsigned long long)Tfull);
+        atomicAdd(&L.stats[kStItems], (unsigned long long)base);
+        if (!a.full_mode) atomicAdd(&L.stats[kStDecisions], (unsigned long long)a.batch * L.H);
+        *L.ticket = 0u;   // ready for the next launch
+    }
+}
+
+// ---------------------------------------------------------------------------
+// match_plan: grid (Hkv, batch), block G warps (warp w = query head g*G + w).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
+{
+    const int g = blockIdx.x, b = blockIdx.y;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = L.G, H = L.H;
+    const int h = g * G + w;
+    const size_t bh = (size_t)b * H + h;
+    const int kvlen = L.kv_len[b];
+    const int m = kvlen + 1;            // 1-based position of the new token (index kvlen)
+
+    // KV append of the new token: warp 0 moves K (lanes 0-15) and V (16-31).
+    if (w == 0) {
+        bool ok = true;
+        const size_t off = kv_block(L, b, g, kvlen >> 4, ok);
+        if (ok) {
+            const __nv_bfloat16 *src = (lane < 16 ? a.k_new : a.v_new) + ((size_t)b * L.Hkv + g) * kD;
+            __nv_bfloat16 *dst = (lane < 16 ? L.k_pool : L.v_pool) + off + (size_t)(kvlen & 15) * kD;
+            reinterpret_cast<uint4 *>(dst)[lane & 15] = reinterpret_cast<const uint4 *>(src)[lane & 15];
+        } else if (lane == 0) {
+            atomicOr(L.err, kErrPage);
+        }
+    }
+    const int slot_new = a.full_mode ? 0 : L.step_ctr[b] % L.ring_len;
+    if (g == 0 && threadIdx.x == 0) {
+        L.m_cur[b] = m;
+        L.slot_cur[b] = slot_new;
+    }
+
+    int lo_h = 0;
+    if (!a.full_mode) {
+        // keep the post-RoPE query for Amend (the caller may reuse its buffer)
+        if (lane < 16)
+            reinterpret_cast<uint4 *>(L.q_stash + bh * kD)[lane] =
+                reinterpret_cast<const uint4 *>(a.q_post + bh * kD)[lane];
+
+        // Match: D_e = ||q~_m - q~_e||^2 over valid entries, fp32, lane owns 4 dims.
+        const float4 q = load_bf16x4(a.q_pre + bh * kD + 4 * lane);
+        const float qn2 = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
+        const int32_t *rpos = L.ring_pos + (size_t)b * L.ring_len;
+        const __nv_bfloat16 *rq = L.ring_q + bh * L.ring_len * kD;
+        int best = -1, best_pos = 0;
+        float bestD = CUDART_INF_F;
+        for (int e = 0; e < L.ring_len; e++) {
+            const int pe = rpos[e];
+            if (pe <= 0) continue;
+            const float4 c = load_bf16x4(rq + (size_t)e * kD + 4 * lane);
+            const float dx = q.x - c.x, dy = q.y - c.y, dz = q.z - c.z, dw = q.w - c.w;
+            const float De = warp_sum(dx * dx + dy * dy + dz * dz + dw * dw);
+            if (best < 0 || De < bestD || (De == bestD && pe > best_pos)) {
+                best = e;
+                bestD = De;
+                best_pos = pe;
+            }
+        }
+        const int hit = best >= 0 && bestD < L.tau2 * qn2;
+        int eff = a.force ? L.forced_slot[bh] : (hit ? best : -1);
+        int p = 0;
+        if (eff >= L.ring_len) eff = -2;
+        if (eff >= 0) {
+            p = rpos[eff];
+            if (p <= 0 || p >= m) eff = -2;
+        }
+        if (eff == -2) {   // a forced slot that holds no entry: treat as a miss, flag it
+            if (lane == 0) atomicOr(L.err, kErrSlot);
+            eff = -1;
+            p = 0;
+        }
+        lo_h = eff >= 0 ? max(0, p - L.band_r) : 0;
+        if (lane == 0) {
+            L.dec_own_slot[bh] = best;
+            L.dec_own_hit[bh] = hit;
+            L.dec_D[bh] = bestD;
+            L.dec_qn2[bh] = qn2;
+            L.dec_slot[bh] = eff;
+            L.dec_lo[bh] = lo_h;
+            if (eff >= 0) atomicAdd(&L.stats[kStHits], 1ull);
+        }
+        // Stage q~_m into the slot this step's Amend completes.  Only this
+        // warp reads this head's ring queries before that Amend has run.
+        __syncwarp();
+        if (lane < 16)
+            reinterpret_cast<uint4 *>(L.ring_q + (bh * L.ring_len + slot_new) * kD)[lane] =
+                reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[lane];
+    } else if (lane == 0) {
+        L.dec_slot[bh] = -1;
+        L.dec_lo[bh] = 0;
+    }
+
+    // group span start = min over the group's heads; then the ticket
+    __shared__ int s_lo[32];
+    __shared__ int s_last;
+    if (lane == 0) s_lo[w] = lo_h;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int lo = s_lo[0];
+        for (int i = 1; i < G; i++) lo = min(lo, s_lo[i]);
+        L.grp_lo[(size_t)b * L.Hkv + g] = lo;
+        __threadfence();
+        const unsigned t = atomicAdd(L.ticket, 1u);
+        s_last = (t == gridDim.x * gridDim.y - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    plan_work(L, a);
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV attention.  CTA = NW warps arranged as NP page lanes x NH head
+// tiles (NH = ceil(G/8)); the warps of one page lane share its S-stage
+// shared-memory pipeline of 16-token pages (K 4 KB + V 4 KB, rows XOR
+// swizzled in 16-byte chunks so ldmatrix is conflict-free).
+//
+// Per page and head tile (8 query heads of the group):
+//   S^T[16 tok x 8 heads] = K[16 x 128] Q^T[128 x 8]   8 x mma m16n8k16
+//   online softmax on the fragments (log2 units)
+//   O^T[128 x 8] += V^T[128 x 16] P^T[16 x 8]          8 x 2 mma (P split
+//   into bf16 hi + lo so P V keeps ~16 bits of P: the partials must be
+//   fp32-accurate because Amend's removal amplifies their error)
+// ---------------------------------------------------------------------------
+template <int NW, int S>
+__global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int G = L.G;
+    const int NH = (G + 7) >> 3;
+    const int NP = NW / NH;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ht = warp % NH, pl = warp / NH;
+    const int gthreads = NH * 32;
+    const int gtid = threadIdx.x - pl * gthreads;
+    uint8_t *lane_smem = smem + (size_t)pl * S * kStageBytes;
+    const int r4 = lane >> 2, c4 = lane & 3;
+    const int n_items = *L.n_items;
+    const float sl2 = L.scale_log2;
+
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int4 item = L.items[it];
+        const int bg = item.x, ilo = item.y, ihi = item.z;
+        const int b = bg / L.Hkv, g = bg - b * L.Hkv;
+
+        // Q^T fragments for head column n = r4 of this tile
+        uint32_t qf[8][2];
+        {
+            const int hn = 8 * ht + r4;
+            if (hn < G) {
+                const uint32_t *qrow =
+                    reinterpret_cast<const uint32_t *>(a.q_post + ((size_t)b * L.H + (size_t)g * G + hn) * kD);
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    qf[kk][0] = qrow[8 * kk + c4];
+                    qf[kk][1] = qrow[8 * kk + 4 + c4];
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) qf[kk][0] = qf[kk][1] = 0u;
+            }
+        }
+        // this thread's two head columns and their first valid token (columns
+        // past the group's heads are computed and discarded: no mask)
+        const int hc0 = 8 * ht + 2 * c4, hc1 = hc0 + 1;
+        const size_t hrow = (size_t)b * L.H + (size_t)g * G;
+        const int lo0 = hc0 < G ? max(ilo, L.dec_lo[hrow + hc0]) : ilo;
+        const int lo1 = hc1 < G ? max(ilo, L.dec_lo[hrow + hc1]) : ilo;
+        const int lo_max = max(lo0, lo1);
+
+        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+        float acc[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+        const int pg0 = ilo >> 4, pg1 = (ihi - 1) >> 4;
+        const int npg = pg1 - pg0 + 1;
+        const int npl = pl < npg ? (npg - pl + NP - 1) / NP : 0;
+
+        auto issue = [&](int k) {
+            const int pg = pg0 + pl + k * NP;
+            uint8_t *st = lane_smem + (k % S) * kStageBytes;
+            bool ok = true;
+            const size_t off = kv_block(L, b, g, pg, ok);
+            if (!ok) {
+                if (gtid == 0) atomicOr(L.err, kErrPage);
+                return;
+            }
+            const char *ksrc = reinterpret_cast<const char *>(L.k_pool + off);
+            const char *vsrc = reinterpret_cast<const char *>(L.v_pool + off);
+            for (int c = gtid; c < 512; c += gthreads) {
+                const int isv = c >> 8, cc = c & 255, row = cc >> 4, ch = cc & 15;
+                const char *src = (isv ? vsrc : ksrc) + row * 256 + ch * 16;
+                cp_async16(smem_u32(st + isv * 4096 + row * 256 + ((ch ^ (row & 7)) << 4)), src);
+            }
+        };
+
+#pragma unroll
+        for (int k = 0; k < S - 1; k++) {
+            if (k < npl) issue(k);
+            cp_async_commit();
+        }
+        for (int k = 0; k < npl; k++) {
+            cp_async_wait<S - 2>();
+            named_bar(1 + pl, gthreads);
+            if (k + S - 1 < npl) issue(k + S - 1);
+            cp_async_commit();
+
+            const uint8_t *Ks = lane_smem + (k % S) * kStageBytes;
+            const uint8_t *Vs = Ks + 4096;
+            const int pg = pg0 + pl + k * NP;
+
+            // S^T = K Q^T
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const uint32_t rbase = smem_u32(Ks + row * 256);
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    const int ch = 2 * kk + (lane >> 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(a0, a1, a2, a3, rbase + ((ch ^ (row & 7)) << 4));
+                    mma_bf16(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                }
+            }
+            // s[0]: token r4 head hc0; s[1]: token r4 head hc1; s[2], s[3]: token r4+8
+            float z0 = s[0] * sl2, z1 = s[1] * sl2, z2 = s[2] * sl2, z3 = s[3] * sl2;
+            const int j0 = pg * 16 + r4, j1 = j0 + 8;
+            if (pg * 16 < lo_max || pg * 16 + 16 > ihi) {
+                if (!(j0 >= lo0 && j0 < ihi)) z0 = -CUDART_INF_F;
+                if (!(j0 >= lo1 && j0 < ihi)) z1 = -CUDART_INF_F;
+                if (!(j1 >= lo0 && j1 < ihi)) z2 = -CUDART_INF_F;
+                if (!(j1 >= lo1 && j1 < ihi)) z3 = -CUDART_INF_F;
+            }
+            float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float bs0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+            const float bs1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+            const float al0 = exp2f(m0 - bs0), al1 = exp2f(m1 - bs1);
+            const float p0 = exp2f(z0 - bs0), p1 = exp2f(z1 - bs1);
+            const float p2 = exp2f(z2 - bs0), p3 = exp2f(z3 - bs1);
+            l0 = l0 * al0 + p0 + p2;
+            l1 = l1 * al1 + p1 + p3;
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al1;
+                acc[i][2] *= al0;
+                acc[i][3] *= al1;
+            }
+            // P^T fragments (hi + lo bf16 parts) via in-register transpose
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+            const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+            const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+            const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+            const uint32_t bh0 = movmatrix_t(bf16x2_bits(h01)), bh1 = movmatrix_t(bf16x2_bits(h23));
+            const uint32_t bl0 = movmatrix_t(bf16x2_bits(e01)), bl1 = movmatrix_t(bf16x2_bits(e23));
+            {
+                const int tok = (lane & 7) + 8 * (lane >> 4);
+                const uint32_t vbase = smem_u32(Vs + tok * 256);
+#pragma unroll
+                for (int mt = 0; mt < 8; mt++) {
+                    const int ch = 2 * mt + ((lane >> 3) & 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(a0, a1, a2, a3, vbase + ((ch ^ (tok & 7)) << 4));
+                    mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
+                    mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+                }
+            }
+        }
+        cp_async_wait<0>();
+        __syncthreads();   // every page lane drained: stage memory is free
+
+        // sum l over the 8 lanes that share a head column
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        }
+        // stage each page lane's partial in shared memory, then merge lanes
+        float *red_o = reinterpret_cast<float *>(smem);                               // [NP][G][D]
+        float2 *red_ml = reinterpret_cast<float2 *>(red_o + (size_t)NP * G * kD);     // [NP][G]
+        if (hc0 < G) {
+            float *o0 = red_o + ((size_t)pl * G + hc0) * kD;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                o0[16 * i + r4] = acc[i][0];
+                o0[16 * i + r4 + 8] = acc[i][2];
+            }
+            if (r4 == 0) red_ml[pl * G + hc0] = make_float2(m0, l0);
+        }
+        if (hc1 < G) {
+            float *o1 = red_o + ((size_t)pl * G + hc1) * kD;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                o1[16 * i + r4] = acc[i][1];
+                o1[16 * i + r4 + 8] = acc[i][3];
+            }
+            if (r4 == 0) red_ml[pl * G + hc1] = make_float2(m1, l1);
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < G * kD; idx += NW * 32) {
+            const int hh = idx / kD, dd = idx - hh * kD;
+            float M = -CUDART_INF_F;
+            for (int q = 0; q < NP; q++) M = fmaxf(M, red_ml[q * G + hh].x);
+            float lsum = 0.f, osum = 0.f;
+            if (M != -CUDART_INF_F) {
+                for (int q = 0; q < NP; q++) {
+                    const float2 ml = red_ml[q * G + hh];
+                    const float wq = exp2f(ml.x - M);
+                    lsum += ml.y * wq;
+                    osum += red_o[((size_t)q * G + hh) * kD + dd] * wq;
+                }
+            }
+            L.part_o[((size_t)it * G + hh) * kD + dd] = osum;
+            if (dd == 0) L.part_ml[(size_t)it * G + hh] = make_float2(M, lsum);
+        }
+        __syncthreads();   // shared memory is reused by the next item's pipeline
+    }
+}
+
+struct Acc {
+    float M, L;
+    float4 O;
+};
+
+__device__ __forceinline__ void acc_add(Acc &A, float M, float Lw, float4 O)
+{
+    const float Mn = fmaxf(A.M, M);
+    if (Mn == -CUDART_INF_F) return;
+    const float a = exp2f(A.M - Mn), c = exp2f(M - Mn);
+    A.L = A.L * a + Lw * c;
+    A.O.x = A.O.x * a + O.x * c;
+    A.O.y = A.O.y * a + O.y * c;
+    A.O.z = A.O.z * a + O.z * c;
+    A.O.w = A.O.w * a + O.w * c;
+    A.M = Mn;
+}
+
+// ---------------------------------------------------------------------------
+// combine: one warp per (request, head).  Merges the group's item partials
+// (segment 0: before the amend band, segment 1: the band) and, on a hit,
+// the ring's AS_{1:p-r}.  Writes out (bf16), lse_out, AS_{1:m} and the
+// direct AS_{1:m-r} for Amend.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
+{
+    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= a.batch * L.H) return;
+    const int b = gw / L.H, h = gw - b * L.H;
+    const int g = h / L.G, hh = h - g * L.G;
+    const int bg = b * L.Hkv + g;
+    Acc pre = {-CUDART_INF_F, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+    Acc band = pre;
+    if (!a.full_mode) {
+        const int eff = L.dec_slot[gw];
+        if (eff >= 0) {
+            const size_t e = (size_t)gw * L.ring_len + eff;
+            const float lse = L.ring_lse[e];
+            if (lse != -CUDART_INF_F)
+                acc_add(pre, lse * kLog2e, 1.f, *reinterpret_cast<const float4 *>(L.ring_o + e * kD + 4 * lane));
+        }
+    }
+    const int off0 = L.grp_item_off[bg], off1 = L.grp_item_off[bg + 1];
+    for (int i = off0; i < off1; i++) {
+        const int seg = L.items[i].w;
+        const float2 ml = L.part_ml[(size_t)i * L.G + hh];
+        const float4 o = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
+        acc_add(seg ? band : pre, ml.x, ml.y, o);
+    }
+    Acc full = pre;
+    acc_add(full, band.M, band.L, band.O);
+    const float inv = 1.f / full.L;
+    const float4 of = make_float4(full.O.x * inv, full.O.y * inv, full.O.z * inv, full.O.w * inv);
+    const float lse = (full.M + log2f(full.L)) * kLn2;
+    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(of.x, of.y), hi2 = __floats2bfloat162_rn(of.z, of.w);
+    *reinterpret_cast<uint2 *>(a.out + (size_t)gw * kD + 4 * lane) = make_uint2(bf16x2_bits(lo2), bf16x2_bits(hi2));
+    if (a.lse_out && lane == 0) a.lse_out[gw] = lse;
+    if (!a.full_mode) {
+        *reinterpret_cast<float4 *>(L.as_full_o + (size_t)gw * kD + 4 * lane) = of;
+        float4 op = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lp = -CUDART_INF_F;
+        if (pre.L > 0.f) {
+            const float ip = 1.f / pre.L;
+            op = make_float4(pre.O.x * ip, pre.O.y * ip, pre.O.z * ip, pre.O.w * ip);
+            lp = (pre.M + log2f(pre.L)) * kLn2;
+        }
+        *reinterpret_cast<float4 *>(L.as_pre_o + (size_t)gw * kD + 4 * lane) = op;
+        if (lane == 0) {
+            L.as_full_lse[gw] = lse;
+            L.as_pre_lse[gw] = lp;
+        }
+    } else if (h == 0 && lane == 0) {
+        L.kv_len[b] = L.m_cur[b];   // the full step has no Amend to commit the length
+    }
+}
+
+// ---------------------------------------------------------------------------
+// amend (side stream): grid (Hkv, batch), block G warps.
+// AS_{m-r+1:m} with q_m (band recompute, fp32), AS_{1:m-r} = AS_{1:m} (-)
+// band, ring insert at the step's slot, then commit position and length.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) amend_kernel(Layout L, StepArgs a)
+{
+    const int g = blockIdx.x, b = blockIdx.y;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = g * L.G + w;
+    const size_t gw = (size_t)b * L.H + h;
+    const int m = L.m_cur[b];
+    const int slot = L.slot_cur[b];
+    const int r = L.band_r;
+    float4 oe = make_float4(0.f, 0.f, 0.f, 0.f);
+    float le = -CUDART_INF_F;
+    if (m > r) {
+        const float4 q = load_bf16x4(L.q_stash + gw * kD + 4 * lane);
+        float M = -CUDART_INF_F, Ls = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool ok = true;
+        for (int j = m - r; j < m; j++) {
+            const size_t off = kv_block(L, b, g, j >> 4, ok) + (size_t)(j & 15) * kD + 4 * lane;
+            if (!ok) break;
+            const float4 k = load_bf16x4(L.k_pool + off);
+            const float z = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w) * L.scale_log2;
+            const float4 v = load_bf16x4(L.v_pool + off);
+            const float Mn = fmaxf(M, z);
+            const float al = exp2f(M - Mn), p = exp2f(z - Mn);
+            Ls = Ls * al + p;
+            O.x = O.x * al + p * v.x;
+            O.y = O.y * al + p * v.y;
+            O.z = O.z * al + p * v.z;
+            O.w = O.w * al + p * v.w;
+            M = Mn;
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(L.err, kErrPage);
+        } else {
+            const float lb = (M + log2f(Ls)) * kLn2;
+            const float lf = L.as_full_lse[gw];
+            const float delta = fminf(lb - lf, 0.f);
+            const float cond = -expm1f(delta);   // 1 - e^delta
+            if (cond < kRemovalMinCond) {
+                oe = *reinterpret_cast<const float4 *>(L.as_pre_o + gw * kD + 4 * lane);
+                le = L.as_pre_lse[gw];
+                if (lane == 0) atomicAdd(&L.stats[kStDirect], 1ull);
+            } else {
+                const float wgt = expf(delta);
+                const float inv_ls = 1.f / Ls, inv_c = 1.f / cond;
+                const float4 of = *reinterpret_cast<const float4 *>(L.as_full_o + gw * kD + 4 * lane);
+                oe = make_float4((of.x - wgt * O.x * inv_ls) * inv_c, (of.y - wgt * O.y * inv_ls) * inv_c,
+                                 (of.z - wgt * O.z * inv_ls) * inv_c, (of.w - wgt * O.w * inv_ls) * inv_c);
+                le = lf + log1mexp_f(delta);
+            }
+        }
+    }
+    const size_t e = gw * L.ring_len + slot;
+    *reinterpret_cast<float4 *>(L.ring_o + e * kD + 4 * lane) = oe;
+    if (lane == 0) L.ring_lse[e] = le;
+    __syncthreads();
+    if (g == 0 && threadIdx.x == 0) {
+        L.ring_pos[(size_t)b * L.ring_len + slot] = m;
+        L.kv_len[b] = m;
+        L.step_ctr[b] = L.step_ctr[b] + 1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// append: n tokens of K and V [n][Hkv][D] at indices start.. of request req.
+// ---------------------------------------------------------------------------
+__global__ void append_kernel(Layout L, int req, int start, int n, const __nv_bfloat16 *k,
+                              const __nv_bfloat16 *v)
+{
+    const size_t per = (size_t)n * L.Hkv * 16;   // 16-byte chunks of K (and of V)
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < 2 * per;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int isv = idx >= per;
+        const size_t c = isv ? idx - per : idx;
+        const int t = (int)(c / ((size_t)L.Hkv * 16));
+        const int rem = (int)(c - (size_t)t * L.Hkv * 16);
+        const int g = rem >> 4, ch = rem & 15;
+        const int tok = start + t;
+        bool ok = true;
+        const size_t off = kv_block(L, req, g, tok >> 4, ok);
+        if (!ok) {
+            atomicOr(L.err, kErrPage);
+            continue;
+        }
+        const uint4 *src = reinterpret_cast<const uint4 *>((isv ? v : k) + ((size_t)t * L.Hkv + g) * kD) + ch;
+        uint4 *dst = reinterpret_cast<uint4 *>((isv ? L.v_pool : L.k_pool) + off + (size_t)(tok & 15) * kD) + ch;
+        *dst = *src;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) L.kv_len[req] = start + n;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+static size_t attention_smem(int G)
+{
+    const int NH = (G + 7) / 8, NP = kAttnWarps / NH;
+    const size_t pipe = (size_t)NP * kAttnStages * kStageBytes;
+    const size_t red = (size_t)NP * G * kD * 4 + (size_t)NP * G * 8;
+    return pipe > red ? pipe : red;
+}
+
+cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm)
+{
+    *smem = attention_smem(G);
+    auto k = attention_kernel<kAttnWarps, kAttnStages>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, k, kAttnWarps * 32, *smem);
+}
+
+cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s)
+{
+    match_plan_kernel<<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)
+{
+    attention_kernel<kAttnWarps, kAttnStages><<<a.grid_ctas, kAttnWarps * 32, smem, s>>>(L, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
+{
+    const int warps = a.batch * L.H;
+    combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(L, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s)
+{
+    amend_kernel<<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(const Layout &L, int req, int start, int n, const __nv_bfloat16 *k,
+                          const __nv_bfloat16 *v, cudaStream_t s)
+{
+    const size_t chunks = (size_t)2 * n * L.Hkv * 16;
+    size_t blocks = (chunks + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    append_kernel<<<(unsigned)blocks, 256, 0, s>>>(L, req, start, n, k, v);
+    return cudaGetLastError();
+}
+
+}  // namespace macgpu
