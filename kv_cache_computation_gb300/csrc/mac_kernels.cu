@@ -144,9 +144,11 @@ __device__ __forceinline__ int n_chunks(int a, int b, int C)
     return b > a ? (b - 1) / C - a / C + 1 : 0;
 }
 
+// x rounded up to a multiple of 16, clamped to 2^30 (the longest request)
 __device__ __forceinline__ int round_up16(long long x)
 {
-    return (int)((x + 15) / 16 * 16);
+    const long long r = (x + 15) / 16 * 16;
+    return (int)(r < (1ll << 30) ? r : (1ll << 30));
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim a multiple of 32,
@@ -181,8 +183,10 @@ __device__ int block_exclusive_scan(int v, int *total)
 
 __device__ __forceinline__ int group_chunk(const StepArgs &a, int s_C, int splits, int lo, int hi, int scale)
 {
-    int C = a.plan_mode == 0 ? s_C : max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
-    return C * scale;
+    const long long C =
+        a.plan_mode == 0 ? s_C : max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
+    const long long Cs = C * scale;
+    return (int)(Cs < (1ll << 30) ? Cs : (1ll << 30));
 }
 
 // ---------------------------------------------------------------------------
@@ -247,7 +251,7 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
         }
         int tot;
         block_exclusive_scan(cnt, &tot);
-        if (tot <= L.item_cap) break;
+        if (tot <= L.item_cap || scale >= (1 << 30)) break;
         scale *= 2;
     }
     // offsets and items; groups are taken in rounds so the list stays in order

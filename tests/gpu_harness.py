@@ -1,0 +1,117 @@
+"""Shared set-up for the GPU parity tests: one MAC handle and one oracle fed
+the same seeded inputs, and the comparison rules.
+
+Tolerances (the method's fixed bar): outputs within 5e-3 of the largest
+reference element of each (request, head) vector (bf16 output, fp32
+accumulation); LSE within 1e-4 absolute; Match decisions identical except
+where the exact distance is within 1e-4 (relative) of the threshold or of
+the runner-up.
+"""
+import numpy as np
+import torch
+
+import oracle
+from kv_cache_computation_gb300 import MacAttention
+from kv_cache_computation_gb300 import workloads as W
+
+OUT_TOL = 5e-3
+LSE_TOL = 1e-4
+KEYS = ("q_pre", "q_post", "k_new", "v_new")
+
+
+def rel_err(got, ref):
+    """max_i |got_i - ref_i| / max_i |ref_i| over the last axis."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return np.abs(got - ref).max(axis=-1) / np.maximum(np.abs(ref).max(axis=-1), 1e-30)
+
+
+def check_out(out, lse, ref, what=""):
+    o = out.float().cpu().numpy()
+    e = rel_err(o, ref["out"])
+    assert e.max() <= OUT_TOL, f"{what} output error {e.max():.3g} at {np.unravel_index(e.argmax(), e.shape)}"
+    if lse is not None:
+        le = np.abs(lse.cpu().numpy().astype(np.float64) - ref["lse"])
+        assert le.max() <= LSE_TOL, f"{what} lse error {le.max():.3g}"
+    return float(e.max())
+
+
+class Pair:
+    """A MAC handle and the oracle over identical inputs."""
+
+    def __init__(self, cfg: W.DecodeConfig, contexts=None, page_size=16, plan_mode=0, extra_steps=0):
+        self.cfg = cfg
+        B = cfg.batch
+        self.contexts = list(contexts) if contexts is not None else [cfg.context] * B
+        self.t_max = max(self.contexts) + cfg.steps + extra_steps
+        K, V = W.prefill_kv(cfg) if cfg.context > 0 else (None, None)
+        self.mac = MacAttention(cfg.heads, cfg.kv_heads, cfg.head_dim, cfg.ring_len, cfg.band_r, cfg.tau,
+                                max_batch=B, max_ctx=self.t_max, page_size=page_size, plan_mode=plan_mode)
+        if page_size:
+            ppr = (self.t_max + 15) // 16
+            self.pages = W.page_tables(B, ppr, seed=cfg.seed).cuda()
+            for b in range(B):
+                self.mac.set_page_table(b, self.pages[b].contiguous())
+        Ko = np.zeros((B, self.t_max, cfg.kv_heads, cfg.head_dim), np.uint16)
+        Vo = np.zeros_like(Ko)
+        for b, n in enumerate(self.contexts):
+            if n > 0:
+                self.mac.append_kv(b, K[b, :n].cuda().contiguous(), V[b, :n].cuda().contiguous())
+                Ko[b, :n] = W.bf16_bits(K[b, :n])
+                Vo[b, :n] = W.bf16_bits(V[b, :n])
+        self.orc = oracle.MacState(Ko, Vo, cfg.heads, cfg.ring_len, cfg.band_r, cfg.tau)
+        for b, n in enumerate(self.contexts):
+            self.orc.reset(b, n)
+        self.inputs = W.decode_inputs(cfg)
+        self.flagged = 0
+
+    def step_inputs(self, t):
+        dev = [self.inputs[k][t].cuda().contiguous() for k in KEYS]
+        host = [W.bf16_bits(self.inputs[k][t]) for k in KEYS]
+        return dev, host
+
+    def mac_step(self, t, force=True, check_ring=True):
+        """One step on both sides; compares decisions, outputs and the ring.
+        With force, the GPU path runs under the oracle's decisions."""
+        dev, host = self.step_inputs(t)
+        ref = self.orc.step(*host)
+        if force:
+            slots = np.where(ref["hit"], ref["slot"], -1).astype(np.int32)
+            self.mac.force_decisions(torch.from_numpy(slots).cuda())
+        out, lse = self.mac.decode_step(*dev)
+        self.mac.sync()
+        dec = self.mac.decisions(self.cfg.batch)
+        flag = oracle.decision_flags(ref["D"], ref["D2"], ref["qn2"], self.cfg.tau)
+        self.flagged += int(flag.sum())
+        ok = (dec["hit"] == ref["hit"]) & (dec["slot"] == ref["slot"])
+        assert (ok | flag).all(), f"step {t}: decisions differ at {np.argwhere(~(ok | flag))[:5].tolist()}"
+        if not force:
+            assert ok.all(), f"step {t}: flagged decision divergence; rerun under forced decisions"
+        err = check_out(out, lse, ref, f"step {t}")
+        if check_ring:
+            self.check_ring(t)
+        return ref, err
+
+    def full_step(self, t):
+        dev, host = self.step_inputs(t)
+        ref = self.orc.full_step(host[1], host[2], host[3])
+        out, lse = self.mac.full_step(*dev[1:])
+        torch.cuda.synchronize()
+        return check_out(out, lse, ref, f"full step {t}")
+
+    def check_ring(self, t):
+        ring = self.orc.ring()
+        for b in range(self.cfg.batch):
+            g = self.mac.read_ring(b)
+            np.testing.assert_array_equal(g["pos"], ring["pos"][b])
+            assert g["kv_len"] == ring["kv_len"][b] and g["steps"] == ring["step"][b]
+            valid = ring["pos"][b] > 0
+            np.testing.assert_array_equal(g["q"][:, valid], ring["q"][b][:, valid])
+            lo, ll = ring["o"][b][:, valid], ring["lse"][b][:, valid]
+            go, gl = g["o"][:, valid], g["lse"][:, valid]
+            empty = ll == -np.inf
+            assert (gl[empty] == -np.inf).all()
+            if (~empty).any():
+                e = rel_err(go[~empty], lo[~empty])
+                assert e.max() <= OUT_TOL, f"step {t} ring o error {e.max():.3g}"
+                assert np.abs(gl[~empty] - ll[~empty]).max() <= LSE_TOL, f"step {t} ring lse error"

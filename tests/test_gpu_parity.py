@@ -1,0 +1,147 @@
+"""GPU parity of the CUDA path against the fp64 oracle, through the C ABI.
+
+Shapes span several KV pages, several work items per group and a ragged
+tail; edge cases cover empty prefill, single tokens, band wider than the
+context, ring length 1, and every GQA/MQA group size.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_computation_gb300 import workloads as W
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kv_cache_computation_gb300 import build
+    build.build()
+
+
+def cfg(**kw):
+    base = dict(name="t", batch=2, heads=32, kv_heads=8, head_dim=128, context=600, steps=12, ring_len=8,
+                band_r=32, tau=0.3, rho=0.99, paged=True)
+    base.update(kw)
+    return W.DecodeConfig(**base)
+
+
+def _pair(c, **kw):
+    from gpu_harness import Pair
+    return Pair(c, **kw)
+
+
+@pytest.mark.parametrize("page_size", [16, 0])
+@pytest.mark.parametrize("context", [1, 15, 300, 2049])
+def test_full_step_matches_oracle(page_size, context):
+    p = _pair(cfg(context=context, steps=3), page_size=page_size)
+    for t in range(3):
+        p.full_step(t)
+
+
+@pytest.mark.parametrize("kv_heads", [32, 16, 8, 4, 2, 1])
+def test_full_step_every_group_size(kv_heads):
+    p = _pair(cfg(kv_heads=kv_heads, context=777, steps=2, batch=2))
+    for t in range(2):
+        p.full_step(t)
+
+
+@pytest.mark.parametrize("page_size", [16, 0])
+@pytest.mark.parametrize("band_r,ring_len", [(32, 8), (64, 16), (16, 1)])
+def test_mac_chain_under_oracle_decisions(page_size, band_r, ring_len):
+    p = _pair(cfg(band_r=band_r, ring_len=ring_len, steps=16), page_size=page_size)
+    hits = 0
+    for t in range(16):
+        ref, _ = p.mac_step(t, force=True)
+        hits += int(ref["hit"].sum())
+    assert hits > 0
+    st = p.mac.stats()
+    assert st["device_error"] == 0 and st["steps"] == 16
+
+
+def test_mac_chain_own_decisions():
+    p = _pair(cfg(steps=16, rho=0.995, ring_len=6))
+    hits = 0
+    for t in range(16):
+        ref, _ = p.mac_step(t, force=False)
+        hits += int(ref["hit"].sum())
+    assert hits > 0
+    st = p.mac.stats()
+    assert st["hits"] == hits and st["head_decisions"] == 16 * 2 * 32
+
+
+@pytest.mark.parametrize("kv_heads", [32, 8, 4, 1])
+def test_mac_chain_group_sizes(kv_heads):
+    p = _pair(cfg(kv_heads=kv_heads, context=500, steps=10, rho=0.995, ring_len=4))
+    for t in range(10):
+        p.mac_step(t, force=True)
+
+
+def test_heterogeneous_rho_and_lengths():
+    c = cfg(batch=3, rho_range=(0.5, 0.999), steps=14, context=900, band_r=64)
+    p = _pair(c, contexts=[900, 40, 333])
+    for t in range(14):
+        p.mac_step(t, force=True)
+
+
+def test_empty_prefill_and_band_wider_than_context():
+    p = _pair(cfg(context=0, steps=20, band_r=64, ring_len=4, rho=0.999))
+    for t in range(20):
+        p.mac_step(t, force=True)
+
+
+def test_tau_zero_never_hits_and_is_full_attention():
+    p = _pair(cfg(tau=0.0, steps=8, rho=0.9999))
+    for t in range(8):
+        ref, _ = p.mac_step(t, force=False)
+        assert not ref["hit"].any()
+    assert p.mac.stats()["hits"] == 0
+
+
+@pytest.mark.parametrize("plan_mode", [0, 1])
+def test_plan_modes_agree_with_oracle(plan_mode):
+    c = cfg(batch=4, rho_range=(0.5, 0.999), steps=8, context=1500)
+    p = _pair(c, plan_mode=plan_mode)
+    for t in range(8):
+        p.mac_step(t, force=True, check_ring=(t == 7))
+
+
+def test_kv_bytes_accounting():
+    c = cfg(steps=6, rho=0.999)
+    p = _pair(c)
+    for t in range(6):
+        p.mac_step(t, force=True, check_ring=False)
+    st = p.mac.stats()
+    full = sum(2 * 8 * (600 + t + 1) for t in range(6))
+    assert st["kv_tokens_full"] == full
+    assert 0 < st["kv_tokens_read"] <= full
+
+
+def test_capacity_and_argument_errors():
+    from kv_cache_computation_gb300 import MacError
+    c = cfg(steps=1, context=20)
+    p = _pair(c)
+    dev, _ = p.step_inputs(0)
+    p.mac.decode_step(*dev)
+    with pytest.raises(MacError) as e:
+        p.mac.decode_step(*dev)                       # max_ctx = context + steps reached
+    assert e.value.status == -4
+    with pytest.raises(MacError):
+        p.mac.append_kv(0, torch.zeros((1, 8, 128), dtype=torch.bfloat16, device="cuda"),
+                        torch.zeros((1, 8, 128), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(TypeError):
+        p.mac.decode_step(dev[0].float(), *dev[1:])
+    p.mac.sync()
+    assert p.mac.stats()["device_error"] == 0
+
+
+def test_reset_request_restarts_cleanly():
+    c = cfg(steps=6, batch=1, context=100)
+    p = _pair(c, extra_steps=200)
+    for t in range(3):
+        p.mac_step(t, force=True, check_ring=False)
+    p.mac.reset_request(0)
+    p.mac.sync()
+    r = p.mac.read_ring(0)
+    assert r["kv_len"] == 0 and r["steps"] == 0 and not r["pos"].any()
