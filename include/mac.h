@@ -113,7 +113,8 @@ mac_status mac_query_sizes(const mac_config *cfg, size_t *kv_bytes, size_t *ring
 
 /* Create a handle over caller-allocated device buffers (each 256-byte
  * aligned and at least the size mac_query_sizes gives; MAC_ERR_OOM if not).
- * Clears rings, lengths and counters; creates the side stream and events.
+ * Zeroes the KV store; clears rings, lengths and counters; creates the side
+ * stream and events.
  * Synchronous. */
 mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void *dev_ring,
                       size_t ring_bytes, void *dev_scratch, size_t scratch_bytes, mac_handle *out);

@@ -408,6 +408,11 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     L.stats = (unsigned long long *)(sc + z.s_stats);
     L.err = (uint32_t *)(sc + z.s_err);
 
+    // Zero the KV store: a page's slots past a request's last token are
+    // streamed (and masked to probability 0) with the rest of the page, and
+    // 0 x NaN from never-written memory would still reach the output.
+    e = cudaMemset(dev_kv, 0, z.kv);
+    if (e != cudaSuccess) return fail(e, "cudaMemset(kv)");
     // zero the scratch (lengths, counters, ticket, page table) and the ring positions
     e = cudaMemset(dev_scratch, 0, z.scratch);
     if (e != cudaSuccess) return fail(e, "cudaMemset(scratch)");

@@ -70,6 +70,9 @@ def lib():
     L.orc_mac_step.restype = ctypes.c_int
     L.orc_mac_step.argtypes = [ctypes.c_void_p, ctypes.c_int, _u16, _u16, _u16, _u16, _d, _d,
                                _i32, _d, _d, _d, _i32, _i64]
+    L.orc_mac_step_heads.restype = ctypes.c_int
+    L.orc_mac_step_heads.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16, _u16, _u16,
+                                     _u16, _d, _d, _i32, _d, _d, _d, _i32, _i64]
     L.orc_full_step.restype = ctypes.c_int
     L.orc_full_step.argtypes = [ctypes.c_void_p, ctypes.c_int, _u16, _u16, _u16, _d, _d]
     _lib = L
@@ -193,10 +196,11 @@ class MacState:
                                 _ptr(kv_len, _i64), _ptr(step, _i64))
         return dict(pos=pos, q=q, o=o, lse=lse, kv_len=kv_len, step=step)
 
-    def step(self, q_pre, q_post, k_new, v_new):
+    def step(self, q_pre, q_post, k_new, v_new, heads=None):
         """One MAC decode step.  q_pre, q_post uint16 [B', H, d]; k_new,
         v_new uint16 [B', Hkv, d].  Returns dict with out [B', H, d], lse
-        [B', H] and the decisions."""
+        [B', H] and the decisions.  ``heads=(lo, hi)`` evaluates only that
+        range of query heads (a timing sample; other entries are undefined)."""
         q_pre, q_post, k_new, v_new = map(_u16c, (q_pre, q_post, k_new, v_new))
         Bp = q_pre.shape[0]
         H, d = self.H, self.d
@@ -210,7 +214,8 @@ class MacState:
         qn2 = np.empty((Bp, H), np.float64)
         hit = np.empty((Bp, H), np.int32)
         p = np.empty((Bp, H), np.int64)
-        rc = lib().orc_mac_step(self._h, Bp, _ptr(q_pre, _u16), _ptr(q_post, _u16), _ptr(k_new, _u16),
+        h_lo, h_hi = (0, H) if heads is None else heads
+        rc = lib().orc_mac_step_heads(self._h, Bp, h_lo, h_hi, _ptr(q_pre, _u16), _ptr(q_post, _u16), _ptr(k_new, _u16),
                                 _ptr(v_new, _u16), _ptr(out, _d), _ptr(lse, _d), _ptr(slot, _i32),
                                 _ptr(D, _d), _ptr(D2, _d), _ptr(qn2, _d), _ptr(hit, _i32), _ptr(p, _i64))
         if rc != 0:

@@ -304,13 +304,16 @@ static int append_new_token(orc_mac *s, int batch, const uint16_t *k_new, const 
  * [batch][H] (the merged AS_{1:m}), and the decision per (request, head):
  * ring slot (-1 none), D, runner-up D2, ||q~||^2, hit, reuse position p.
  * Returns 0, or a negative code on bad arguments / a full KV store.
+ * orc_mac_step_heads evaluates only query heads [h_lo, h_hi) (a timing
+ * sample); the others' outputs, decisions and ring entries are left as they
+ * were, while lengths, positions and step counters advance as usual.
  */
-int orc_mac_step(orc_mac *s, int batch, const uint16_t *q_pre, const uint16_t *q_post,
-                 const uint16_t *k_new, const uint16_t *v_new, double *out_o, double *out_lse,
-                 int32_t *dec_slot, double *dec_D, double *dec_D2, double *dec_qn2,
-                 int32_t *dec_hit, int64_t *dec_p)
+int orc_mac_step_heads(orc_mac *s, int batch, int h_lo, int h_hi, const uint16_t *q_pre,
+                       const uint16_t *q_post, const uint16_t *k_new, const uint16_t *v_new,
+                       double *out_o, double *out_lse, int32_t *dec_slot, double *dec_D,
+                       double *dec_D2, double *dec_qn2, int32_t *dec_hit, int64_t *dec_p)
 {
-    if (batch < 1 || batch > s->B) return -1;
+    if (batch < 1 || batch > s->B || h_lo < 0 || h_hi > s->H || h_lo >= h_hi) return -1;
     int rc = append_new_token(s, batch, k_new, v_new);
     if (rc) return rc;
     const int H = s->H, d = s->d, L = s->L, G = s->H / s->Hkv;
@@ -321,6 +324,7 @@ int orc_mac_step(orc_mac *s, int batch, const uint16_t *q_pre, const uint16_t *q
 #pragma omp parallel for schedule(dynamic, 1) reduction(+ : n_direct)
     for (long bh = 0; bh < (long)batch * H; bh++) {
         const int b = (int)(bh / H), h = (int)(bh % H), g = h / G;
+        if (h < h_lo || h >= h_hi) continue;             /* heads outside the sample */
         const long m = s->kv_len[b] + 1;                 /* 1-based position of the new token */
         const long slot_new = (long)(s->step[b] % L);    /* R5 */
         const uint16_t *Kh = s->K + (long)b * s->t_max * row + (long)g * d;
@@ -396,6 +400,15 @@ int orc_mac_step(orc_mac *s, int batch, const uint16_t *q_pre, const uint16_t *q
     }
     s->n_direct += n_direct;
     return 0;
+}
+
+int orc_mac_step(orc_mac *s, int batch, const uint16_t *q_pre, const uint16_t *q_post,
+                 const uint16_t *k_new, const uint16_t *v_new, double *out_o, double *out_lse,
+                 int32_t *dec_slot, double *dec_D, double *dec_D2, double *dec_qn2,
+                 int32_t *dec_hit, int64_t *dec_p)
+{
+    return orc_mac_step_heads(s, batch, 0, s->H, q_pre, q_post, k_new, v_new, out_o, out_lse,
+                              dec_slot, dec_D, dec_D2, dec_qn2, dec_hit, dec_p);
 }
 
 /* Full attention decode step (the miss path for every head, no ring): append

@@ -37,8 +37,7 @@ MUTANTS = {
     "values_from_keys": ("const uint16_t *v = V + j * tok_stride;", "const uint16_t *v = K + j * tok_stride;"),
     "ring_slot_shift": ("const long slot_new = (long)(s->step[b] % L);",
                         "const long slot_new = (long)((s->step[b] + 1) % L);"),
-    "kv_head_index": ("const int b = (int)(bh / H), h = (int)(bh % H), g = h / G;\n        const long m = s->kv_len[b] + 1;                 /* 1-based",
-                      "const int b = (int)(bh / H), h = (int)(bh % H), g = h % s->Hkv;\n        const long m = s->kv_len[b] + 1;                 /* 1-based"),
+    "kv_head_index": ("g = h / G;\n        if (h < h_lo", "g = h % s->Hkv;\n        if (h < h_lo"),
     "reuse_prefix_dropped": ("orc_merge(s->ring_o + (ring_base + e) * d, s->ring_lse[ring_base + e], ot, lt, d, o, &l);",
                              "memcpy(o, ot, (size_t)d * sizeof(double)); l = lt;"),
 }
