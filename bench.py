@@ -1,0 +1,421 @@
+"""Benchmark of the MAC-Attention decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--band-r R]
+
+A step is one MAC decode step (KV append, Match, planning, split-KV
+Complete, merge, Amend) for every request of the workload, on inputs already
+resident in HBM.  The default workload is the 128K-context one the metric is
+quoted on: 1 request x 131072 tokens, 32 q / 8 KV heads, d 128, bf16 paged KV
+(page 16, random page permutation), per-head AR(1) rho ~ U[0.5, 0.99], ring
+32, r 64, tau 0.3.  KV (537 MB) is larger than L2, so no flush is needed.
+
+Rank 0 prints one JSON line.  N > 1 runs independent replicas (one process
+per GPU, no collective on the data path; the path has no exchange step).
+
+--impl reference times the fp64 CPU oracle on the host cores on the same
+workload, metric and unit (each step a bounded sample of query heads, scaled
+to the whole step).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn us/step & HBM GB/s (frac of 8 TB/s) at 128K ctx; KV bytes read vs full"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+BYTES_PER_KV_TOKEN = 128 * 2 * 2        # K + V, bf16, d = 128, one KV head
+
+
+def workload(name, band_r, steps):
+    from kv_cache_computation_gb300 import workloads as W
+    table = {
+        "gqa_128k_b1_hetero": lambda: W.llama_gqa_128k_b1_hetero(steps=steps, band_r=band_r),
+        "gqa_32k_b8_paged": lambda: W.llama_gqa_32k_b8_paged(steps=steps),
+        "gqa_4k_b1_contig": lambda: W.llama_gqa_4k_b1_contig(steps=steps),
+    }
+    if name not in table:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(table)}")
+    return table[name]()
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_file):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "attention_kernel_128k.md")
+    if not os.path.exists(prof):
+        return None
+    with open(kernel_file, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    vals = {}
+    for ln in open(prof):
+        if ln.startswith("traffic_bytes_per_launch:") or ln.startswith("kernel_source_sha256_16:"):
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = str(device_index)
+        try:   # nvidia-smi ignores CUDA_VISIBLE_DEVICES: address the GPU by UUID
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.idx = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mac_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def host_inputs(inp, t, keys=("q_pre", "q_post", "k_new", "v_new")):
+    from kv_cache_computation_gb300 import workloads as W
+    return [W.bf16_bits(inp[k][t]) for k in keys]
+
+
+def run_oracle(cfg, K_dev, V_dev, inp, budget_s, max_steps, fixed_steps=None, warm=0):
+    """Time the fp64 oracle on the host cores on this workload.
+
+    Calibrates on one whole step, then times either ``fixed_steps`` steps
+    (each a sample of query heads sized so the run fits ``budget_s``) or as
+    many whole steps as fit ``budget_s`` (2 .. max_steps).  Returns (us per
+    whole step, OpenMP threads, description of the sample)."""
+    import oracle
+    from kv_cache_computation_gb300 import workloads as W
+    B, H = cfg.batch, cfg.heads
+    n_need = warm + 1 + (fixed_steps if fixed_steps else max_steps)
+    t_max = cfg.context + n_need + 1
+    Ko = np.zeros((B, t_max, cfg.kv_heads, cfg.head_dim), np.uint16)
+    Vo = np.zeros_like(Ko)
+    Ko[:, :cfg.context] = W.bf16_bits(K_dev)
+    Vo[:, :cfg.context] = W.bf16_bits(V_dev)
+    st = oracle.MacState(Ko, Vo, H, cfg.ring_len, cfg.band_r, cfg.tau)
+    for b in range(B):
+        st.reset(b, cfg.context)
+    t = 0
+    for _ in range(warm):
+        st.step(*host_inputs(inp, t))
+        t += 1
+    t0 = time.perf_counter()
+    st.step(*host_inputs(inp, t))
+    full_s = time.perf_counter() - t0
+    t += 1
+    heads = H
+    if fixed_steps:
+        n = fixed_steps
+        while heads > 1 and n * full_s * heads / H > budget_s:
+            heads //= 2
+    else:
+        n = int(min(max_steps, max(2, budget_s // max(full_s, 1e-9))))
+        while heads > 1 and n * full_s * heads / H > budget_s:
+            heads //= 2
+    t0 = time.perf_counter()
+    for _ in range(n):
+        st.step(*host_inputs(inp, t), heads=(0, heads))
+        t += 1
+    el = time.perf_counter() - t0
+    us = el / n * 1e6 * (H / heads)
+    sample = (f"{n} decode steps of this workload on the fp64 oracle"
+              + ("" if heads == H else f", query heads 0..{heads - 1} of {H} per step, scaled x{H // heads} "
+                                       "to a whole step")
+              + f"; {el:.1f} s of CPU time")
+    return us, oracle.num_threads(), sample
+
+
+def bench_ours(args, ws, rank, local):
+    from kv_cache_computation_gb300 import MacAttention
+    from kv_cache_computation_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K_steps, W_steps = args.steps, args.warmup
+    total_steps = W_steps + 2 * K_steps + 2
+    cfg = workload(args.workload, args.band_r, total_steps)
+    B, H, Hkv, G = cfg.batch, cfg.heads, cfg.kv_heads, cfg.group
+
+    Kp, Vp = W.prefill_kv(cfg, device=dev)
+    inp = W.decode_inputs(cfg, device=dev)
+    max_ctx = cfg.context + total_steps
+    page = 16 if cfg.paged else 0
+    mac = MacAttention(H, Hkv, cfg.head_dim, cfg.ring_len, cfg.band_r, cfg.tau, max_batch=B, max_ctx=max_ctx,
+                       page_size=page, plan_mode=args.plan_mode)
+    if page:
+        ppr = (max_ctx + 15) // 16
+        pt = W.page_tables(B, ppr, seed=cfg.seed).to(dev)
+        for b in range(B):
+            mac.set_page_table(b, pt[b].contiguous())
+    for b in range(B):
+        mac.append_kv(b, Kp[b].contiguous(), Vp[b].contiguous())
+    out = torch.empty((B, H, cfg.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    step_args = lambda t: (inp["q_pre"][t], inp["q_post"][t], inp["k_new"][t], inp["v_new"][t])
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for t in range(W_steps):
+        mac.decode_step(*step_args(t), out=out, lse=lse)
+    mac.sync()
+    torch.cuda.synchronize()
+    mac.reset_stats()
+    mac.set_profiling(True)
+
+    # timed region: K steps, device events on the launching stream
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for t in range(W_steps, W_steps + K_steps):
+            mac.decode_step(*step_args(t), out=out, lse=lse)
+        mac.join()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    ms = e0.elapsed_time(e1)
+    prof = mac.profile()
+    mac.set_profiling(False)
+    st = mac.stats()
+    clk = clocks.summary()
+    ms_max = max_over_ranks(ms, ws, dev)
+    us_step = ms_max * 1e3 / K_steps
+
+    # end to end through the C ABI with host (pinned) buffers
+    pin = lambda x: x.cpu().pin_memory()
+    h_in = {k: pin(inp[k][W_steps + K_steps:W_steps + 2 * K_steps]) for k in ("q_pre", "q_post", "k_new", "v_new")}
+    d_in = [torch.empty_like(inp[k][0]) for k in ("q_pre", "q_post", "k_new", "v_new")]
+    h_out = torch.empty((B, H, cfg.head_dim), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for i in range(K_steps):
+        for d, k in zip(d_in, ("q_pre", "q_post", "k_new", "v_new")):
+            d.copy_(h_in[k][i], non_blocking=True)
+        mac.decode_step(*d_in, out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+    mac.join()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = max_over_ranks(e2.elapsed_time(e3), ws, dev) * 1e3 / K_steps
+    h2d = sum(x[0].numel() * x.element_size() for x in h_in.values())
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    # bytes
+    kv_read = st["kv_tokens_read"] * BYTES_PER_KV_TOKEN
+    kv_full = st["kv_tokens_full"] * BYTES_PER_KV_TOKEN
+    steps = st["steps"]
+    items = st["work_items"]
+    partial = items * G * (128 * 4 + 8)
+    attn_bytes = kv_read + steps * B * H * 256 + partial
+    L = cfg.ring_len
+    ring = steps * B * H * L * 256 + st["hits"] * (128 * 4 + 4)
+    io = steps * (B * H * 256 * 2 + B * Hkv * 512 + B * H * 256 + B * H * 4) + 2 * partial
+    amend_w = steps * B * H * (256 + 128 * 4 + 4)
+    step_bytes = kv_read + ring + io + amend_w
+    hbm_gbs = step_bytes / (ms * 1e-3) / 1e9
+    attn_s = prof["attention_ms"] * 1e-3
+    peak, peak_kind = measured_peaks()
+    achieved = attn_bytes / attn_s / 1e9 if attn_s > 0 else None
+    traffic = profiled_traffic(os.path.join(ROOT, "kv_cache_computation_gb300", "csrc", "mac_kernels.cu"))
+    launches = prof["steps"] or steps
+
+    result = {
+        "metric": METRIC, "value": round(us_step, 3), "unit": "us/step", "n_gpus": ws, "steps": K_steps,
+        "warmup": W_steps, "ms_per_step": round(us_step / 1e3, 6), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": B, "context": cfg.context, "heads": H, "kv_heads": Hkv,
+                   "head_dim": cfg.head_dim, "ring_len": L, "band_r": cfg.band_r, "tau": cfg.tau,
+                   "page_size": page, "plan_mode": args.plan_mode, "accumulate": "fp32",
+                   "l2": f"inputs larger than L2 (KV {B * Hkv * cfg.context * BYTES_PER_KV_TOKEN / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "tokens_per_s": round(sum_over_ranks(B, ws, dev) / (us_step * 1e-6), 1),
+        "hbm_gbs_step": round(hbm_gbs, 1),
+        "hbm_frac_of_8tbs": round(hbm_gbs / NOMINAL_HBM_GBS, 4),
+        "kv_bytes_read_vs_full": round(kv_read / kv_full, 5) if kv_full else None,
+        "hit_rate": round(st["hits"] / max(1, st["head_decisions"]), 5),
+        "phase_us_per_step": {k.replace("_ms", ""): round(v * 1e3 / launches, 3) for k, v in prof.items()
+                              if k.endswith("_ms")},
+        "roofline": {"kernel": "attention_kernel", "bound": "hbm",
+                     "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4) if achieved else None,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": round(attn_bytes / launches),
+                     "avg_launch_us": round(attn_s / launches * 1e6, 3),
+                     "traffic": traffic},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(4 * K_steps),
+        "clocks": clk,
+        "stats": {"removal_direct": st["removal_direct"], "device_error": st["device_error"],
+                  "work_items_per_step": round(items / max(1, steps), 1)},
+    }
+    mac.sync()
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        us, cores, sample = run_oracle(cfg, Kp, Vp, inp, args.cpu_budget, max_steps=min(K_steps, 256))
+        result["cpu_baseline"] = {"value": round(us, 1), "unit": "us/step", "cores": cores, "kind": "oracle",
+                                  "sample": sample}
+    mac.close()
+    return result
+
+
+def bench_reference(args, ws, rank, local):
+    """The fp64 oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    from kv_cache_computation_gb300 import workloads as W
+    K_steps, W_steps = args.steps, args.warmup
+    cfg = workload(args.workload, args.band_r, W_steps + K_steps + 4)
+    Kp, Vp = W.prefill_kv(cfg)
+    inp = W.decode_inputs(cfg)
+    us, cores, sample = run_oracle(cfg, Kp, Vp, inp, args.ref_budget, max_steps=K_steps, fixed_steps=K_steps,
+                                   warm=W_steps)
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": ws,
+            "steps": K_steps, "warmup": W_steps, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": cfg.batch, "context": cfg.context, "heads": cfg.heads,
+                       "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "ring_len": cfg.ring_len,
+                       "band_r": cfg.band_r, "tau": cfg.tau},
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_128k_b1_hetero")
+    ap.add_argument("--band-r", type=int, default=64)
+    ap.add_argument("--plan-mode", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        res = bench_reference(args, ws, rank, local)
+    else:
+        res = bench_ours(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
