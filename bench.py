@@ -244,7 +244,7 @@ def bench_ours(args, ws, rank, local):
     max_ctx = cfg.context + total_steps
     page = 16 if cfg.paged else 0
     mac = MacAttention(H, Hkv, cfg.head_dim, cfg.ring_len, cfg.band_r, cfg.tau, max_batch=B, max_ctx=max_ctx,
-                       page_size=page, plan_mode=args.plan_mode)
+                       page_size=page, plan_mode=args.plan_mode, amend_band=args.amend_band)
     if page:
         ppr = (max_ctx + 15) // 16
         pt = W.page_tables(B, ppr, seed=cfg.seed).to(dev)
@@ -333,7 +333,8 @@ def bench_ours(args, ws, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.name, "batch": B, "context": cfg.context, "heads": H, "kv_heads": Hkv,
                    "head_dim": cfg.head_dim, "ring_len": L, "band_r": cfg.band_r, "tau": cfg.tau,
-                   "page_size": page, "plan_mode": args.plan_mode, "accumulate": "fp32",
+                   "page_size": page, "plan_mode": args.plan_mode, "amend_band": args.amend_band,
+                   "accumulate": "fp32",
                    "l2": f"inputs larger than L2 (KV {B * Hkv * cfg.context * BYTES_PER_KV_TOKEN / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "tokens_per_s": round(sum_over_ranks(B, ws, dev) / (us_step * 1e-6), 1),
@@ -398,7 +399,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_128k_b1_hetero")
     ap.add_argument("--band-r", type=int, default=64)
-    ap.add_argument("--plan-mode", type=int, default=0)
+    ap.add_argument("--plan-mode", type=int, default=0, help="0 span-proportional, 1 equal split per group")
+    ap.add_argument("--amend-band", type=int, default=0,
+                    help="0 reuse Complete's band summary, 1 recompute the band in Amend")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -77,6 +77,11 @@ typedef struct {
     int plan_mode;      /* 0: span-proportional work split (the paper's          */
                         /* load-balanced planning, Figure 3(b)); 1: equal split  */
                         /* per KV group regardless of span (unbalanced baseline) */
+    int amend_band;     /* where Amend's rectification term AS_{m-r+1:m} comes   */
+                        /* from: 0 = the band segment Complete already streams   */
+                        /* (the band lies inside band+tail and inside [1, m]);   */
+                        /* 1 = recomputed by the Amend kernel from the KV store  */
+                        /* (Figure 2(c) as drawn).  Same value either way.       */
 } mac_config;
 
 /* Cumulative device counters (mac_get_stats). */

@@ -25,7 +25,7 @@ _psz = ctypes.POINTER(ctypes.c_size_t)
 class MacConfig(ctypes.Structure):
     _fields_ = [("heads", _i), ("kv_heads", _i), ("head_dim", _i), ("ring_len", _i), ("band_r", _i),
                 ("tau", _d), ("max_batch", _i), ("max_ctx", _i64), ("page_size", _i), ("num_pages", _i),
-                ("sm_scale", _f), ("plan_mode", _i)]
+                ("sm_scale", _f), ("plan_mode", _i), ("amend_band", _i)]
 
 
 class MacStats(ctypes.Structure):

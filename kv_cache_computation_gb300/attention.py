@@ -40,9 +40,9 @@ def _dev(t: torch.Tensor, name, dtype, shape=None):
 
 
 def make_config(heads, kv_heads, head_dim, ring_len, band_r, tau, max_batch, max_ctx, page_size=16,
-                num_pages=0, sm_scale=0.0, plan_mode=0) -> N.MacConfig:
+                num_pages=0, sm_scale=0.0, plan_mode=0, amend_band=0) -> N.MacConfig:
     return N.MacConfig(heads, kv_heads, head_dim, ring_len, band_r, float(tau), max_batch, int(max_ctx),
-                       page_size, num_pages, float(sm_scale), plan_mode)
+                       page_size, num_pages, float(sm_scale), plan_mode, amend_band)
 
 
 def query_sizes(cfg: N.MacConfig):
@@ -62,9 +62,9 @@ class MacAttention:
     """
 
     def __init__(self, heads, kv_heads, head_dim=128, ring_len=16, band_r=64, tau=0.3, max_batch=1,
-                 max_ctx=4096, page_size=16, num_pages=0, sm_scale=0.0, plan_mode=0, device=None):
+                 max_ctx=4096, page_size=16, num_pages=0, sm_scale=0.0, plan_mode=0, amend_band=0, device=None):
         self.cfg = make_config(heads, kv_heads, head_dim, ring_len, band_r, tau, max_batch, max_ctx, page_size,
-                               num_pages, sm_scale, plan_mode)
+                               num_pages, sm_scale, plan_mode, amend_band)
         self.heads, self.kv_heads, self.head_dim = heads, kv_heads, head_dim
         self.ring_len, self.max_batch, self.band_r, self.tau = ring_len, max_batch, band_r, tau
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

@@ -47,7 +47,7 @@ struct Sizes {
     size_t r_pos, r_q, r_o, r_lse;
     size_t s_page, s_kvlen, s_step, s_mcur, s_slot, s_own_slot, s_own_hit, s_dslot, s_dlo, s_dD, s_dqn2,
         s_forced, s_qstash, s_glo, s_goff, s_items, s_nitems, s_ticket, s_po, s_pml, s_afo, s_afl, s_apo,
-        s_apl, s_stats, s_err;
+        s_apl, s_abo, s_abl, s_stats, s_err;
 };
 
 bool valid_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16 || G == 32; }
@@ -68,6 +68,7 @@ mac_status compute_sizes(const mac_config *c, Sizes *z)
     if (c->num_pages < 0) return MAC_ERR_INVALID_ARG;
     if (!(c->sm_scale >= 0.f) || !std::isfinite(c->sm_scale)) return MAC_ERR_INVALID_ARG;
     if (c->plan_mode != 0 && c->plan_mode != 1) return MAC_ERR_INVALID_ARG;
+    if (c->amend_band != 0 && c->amend_band != 1) return MAC_ERR_INVALID_ARG;
 
     const size_t B = c->max_batch, H = c->heads, Hkv = c->kv_heads, L = c->ring_len;
     z->G = G;
@@ -91,7 +92,7 @@ mac_status compute_sizes(const mac_config *c, Sizes *z)
     z->r_lse = r.take(B * H * L * 4);
     z->ring = r.off;
 
-    z->item_cap = kMaxCtas + 4 * (int)(B * Hkv);
+    z->item_cap = 2 * kMaxCtas + 4 * (int)(B * Hkv);
     const size_t cap = z->item_cap, BH = B * H, BG = B * Hkv;
     Carver s;
     z->s_page = s.take(B * (size_t)z->pages_per_req * 4);
@@ -118,6 +119,8 @@ mac_status compute_sizes(const mac_config *c, Sizes *z)
     z->s_afl = s.take(BH * 4);
     z->s_apo = s.take(BH * kD * 4);
     z->s_apl = s.take(BH * 4);
+    z->s_abo = s.take(BH * kD * 4);
+    z->s_abl = s.take(BH * 4);
     z->s_stats = s.take(kStCount * 8);
     z->s_err = s.take(4);
     z->scratch = s.off;
@@ -356,6 +359,8 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     e = attention_kernel_config(z.G, &h->attn_smem, &per_sm);
     if (e != cudaSuccess) return fail(e, "attention kernel configuration");
     if (per_sm < 1) return fail(cudaErrorInvalidConfiguration, "attention kernel occupancy");
+    e = amend_kernel_config();
+    if (e != cudaSuccess) return fail(e, "amend kernel configuration");
     h->grid_ctas = prop.multiProcessorCount * per_sm;
     if (h->grid_ctas > kMaxCtas) h->grid_ctas = kMaxCtas;
 
@@ -405,6 +410,9 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     L.as_full_lse = (float *)(sc + z.s_afl);
     L.as_pre_o = (float *)(sc + z.s_apo);
     L.as_pre_lse = (float *)(sc + z.s_apl);
+    L.as_band_o = (float *)(sc + z.s_abo);
+    L.as_band_lse = (float *)(sc + z.s_abl);
+    L.amend_band = cfg->amend_band;
     L.stats = (unsigned long long *)(sc + z.s_stats);
     L.err = (uint32_t *)(sc + z.s_err);
 

@@ -20,6 +20,9 @@ constexpr int kAttnStages = 3;          // pipeline stages per page lane
 constexpr int kStageBytes = 2 * kPage * kD * 2;   // one K page + one V page (bf16): 8 KB
 constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
 constexpr int kMinChunk = 64;           // smallest work-item span in tokens
+constexpr int kPlanCache = 1024;        // groups the planner caches in shared memory
+constexpr int kBandTile = 64;           // tokens per shared-memory tile of the Amend band recompute
+constexpr int kBandRow = 272;           // padded bytes per staged K/V row (conflict-free per-lane rows)
 
 // device error bits
 enum : uint32_t { kErrPage = 1u, kErrSlot = 2u, kErrPos = 4u };
@@ -36,6 +39,7 @@ struct Layout {
     int num_pages;            // paged: pool pages
     int ctx_stride;           // contiguous: tokens reserved per (request, kv-head)
     int item_cap;
+    int amend_band;           // 0: reuse Complete's band summary; 1: recompute it in Amend
     float tau2;               // tau^2 (fp32)
     float scale_log2;         // sm_scale * log2(e)
 
@@ -74,6 +78,7 @@ struct Layout {
     // merged summaries kept for Amend
     float *as_full_o, *as_full_lse;   // AS_{1:m}
     float *as_pre_o, *as_pre_lse;     // AS_{1:m-r} formed directly (fallback of the removal)
+    float *as_band_o, *as_band_lse;   // AS_{m-r+1:m} from Complete's band segment
 
     unsigned long long *stats;        // [kStCount]
     uint32_t *err;
@@ -98,5 +103,6 @@ cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_append(const Layout &L, int req, int start, int n, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, cudaStream_t s);
 cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm);
+cudaError_t amend_kernel_config();
 
 }  // namespace macgpu

@@ -181,91 +181,126 @@ __device__ int block_exclusive_scan(int v, int *total)
     return before;
 }
 
-__device__ __forceinline__ int group_chunk(const StepArgs &a, int s_C, int splits, int lo, int hi, int scale)
+__device__ __forceinline__ int warp_sum_int(int v)
 {
-    const long long C =
-        a.plan_mode == 0 ? s_C : max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
-    const long long Cs = C * scale;
-    return (int)(Cs < (1ll << 30) ? Cs : (1ll << 30));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
 }
 
 // ---------------------------------------------------------------------------
-// Planning (last block of match_plan).  Per (request, kv-head) group, the
-// streamed span is [lo_g, m) with lo_g the smallest band+tail start of the
-// group's heads; Amend's band [m-r, m) is cut off as its own segment so the
-// direct form of AS_{1:m-r} is available to Amend.  Chunks are cut at
-// multiples of C (a multiple of 16: page aligned).  Balanced mode picks C so
-// the whole step splits into about one item per attention CTA -- longer
-// spans get proportionally more CTAs (Figure 3(b)); equal mode gives every
+// Planning (last block of match_plan).  Per (request, kv-head) group the
+// streamed span is [lo_g, m), lo_g being the smallest band+tail start of the
+// group's heads.  Amend's band [m-r, m) is cut off as its own segment, so
+// Complete yields the rectification term AS_{m-r+1:m} and the direct form of
+// AS_{1:m-r} as by-products.  Chunks are cut at multiples of C (a multiple of
+// 16: page aligned).
+//
+// Balanced mode (Figure 3(b), "load-balanced planning"): every item costs at
+// most C tokens, so the step finishes when the longest item does; the plan
+// takes the smallest C for which the items fit one wave of the persistent
+// attention grid (or k waves when there are more segments than CTAs).
+// Longer spans thereby get proportionally more CTAs.  Equal mode gives every
 // group the same number of items whatever its span (unbalanced baseline).
 // ---------------------------------------------------------------------------
 __device__ void plan_work(const Layout &L, const StepArgs &a)
 {
+    __shared__ int s_lo[kPlanCache], s_sp[kPlanCache], s_hi[kPlanCache];
+    __shared__ int s_C;
+    __shared__ long long s_T, s_Tf;
     const int nbg = a.batch * L.Hkv;
     const int nthr = blockDim.x;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    long long T = 0, Tfull = 0;
-    for (int bg = threadIdx.x; bg < nbg; bg += nthr) {
-        int b = bg / L.Hkv;
-        int hi = __ldcg(&L.kv_len[b]) + 1;
-        int lo = __ldcg(&L.grp_lo[bg]);
-        T += hi - lo;
-        Tfull += hi;
-    }
-    __shared__ long long red_t[32], red_f[32];
-    __shared__ int s_C;
-    for (int o = 16; o; o >>= 1) {
-        T += __shfl_xor_sync(0xffffffffu, T, o);
-        Tfull += __shfl_xor_sync(0xffffffffu, Tfull, o);
-    }
-    if (lane == 0) {
-        red_t[w] = T;
-        red_f[w] = Tfull;
+    const bool cached = nbg <= kPlanCache;
+    auto group = [&](int bg, int &lo, int &sp, int &hi) {
+        if (cached) {
+            lo = s_lo[bg];
+            sp = s_sp[bg];
+            hi = s_hi[bg];
+            return;
+        }
+        hi = __ldcg(&L.kv_len[bg / L.Hkv]) + 1;
+        lo = __ldcg(&L.grp_lo[bg]);
+        sp = a.full_mode ? lo : max(lo, hi - L.band_r);
+    };
+    if (cached) {
+        for (int bg = threadIdx.x; bg < nbg; bg += nthr) {
+            const int hi = __ldcg(&L.kv_len[bg / L.Hkv]) + 1;
+            const int lo = __ldcg(&L.grp_lo[bg]);
+            s_lo[bg] = lo;
+            s_hi[bg] = hi;
+            s_sp[bg] = a.full_mode ? lo : max(lo, hi - L.band_r);
+        }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        long long st = 0, sf = 0;
-        for (int i = 0; i < (nthr >> 5); i++) {
-            st += red_t[i];
-            sf += red_f[i];
+    const int splits = a.grid_ctas / nbg > 1 ? a.grid_ctas / nbg : 1;
+    if (w == 0) {
+        long long T = 0, Tf = 0;
+        int nseg = 0;
+        for (int bg = lane; bg < nbg; bg += 32) {
+            int lo, sp, hi;
+            group(bg, lo, sp, hi);
+            T += hi - lo;
+            Tf += hi;
+            nseg += (sp > lo) + (hi > sp);
         }
-        T = st;
-        Tfull = sf;
-        int C = round_up16((T + a.grid_ctas - 1) / a.grid_ctas);
-        s_C = C < kMinChunk ? kMinChunk : C;
+        for (int o = 16; o; o >>= 1) {
+            T += __shfl_xor_sync(0xffffffffu, T, o);
+            Tf += __shfl_xor_sync(0xffffffffu, Tf, o);
+        }
+        nseg = warp_sum_int(nseg);
+        int C = kMinChunk;
+        if (a.plan_mode == 0) {
+            auto count = [&](int Cc) {
+                int c = 0;
+                for (int bg = lane; bg < nbg; bg += 32) {
+                    int lo, sp, hi;
+                    group(bg, lo, sp, hi);
+                    c += n_chunks(lo, sp, Cc) + n_chunks(sp, hi, Cc);
+                }
+                return warp_sum_int(c);
+            };
+            const long long P = a.grid_ctas;
+            long long Q = (4ll * nseg <= P) ? P : P * (1 + (2ll * nseg + P - 1) / P);
+            if (Q > L.item_cap) Q = L.item_cap;
+            // count(C) < T/C + 2 nseg, so C >= T / (Q - 2 nseg) always fits Q items
+            long long c_lo = round_up16((T + Q - 1) / Q);
+            long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg))
+                                            : (1ll << 30);
+            if (c_lo < kMinChunk) c_lo = kMinChunk;
+            if (c_hi < c_lo) c_hi = c_lo;
+            while (c_lo < c_hi) {
+                long long mid = (c_lo + c_hi) / 2 / 16 * 16;
+                if (mid < c_lo) mid = c_lo;
+                if (count((int)mid) <= Q) c_hi = mid;
+                else c_lo = mid + 16;
+            }
+            C = (int)c_hi;
+        }
+        if (lane == 0) {
+            s_C = C;
+            s_T = T;
+            s_Tf = Tf;
+        }
     }
     __syncthreads();
     const int sC = s_C;
-    const int splits = a.grid_ctas / nbg > 1 ? a.grid_ctas / nbg : 1;
-    int scale = 1;
-    // counts, growing C until the list fits the partial buffers
-    for (int iter = 0; iter < 40; iter++) {
-        int cnt = 0;
-        for (int bg = threadIdx.x; bg < nbg; bg += nthr) {
-            int b = bg / L.Hkv;
-            int hi = __ldcg(&L.kv_len[b]) + 1;
-            int lo = __ldcg(&L.grp_lo[bg]);
-            int split = a.full_mode ? lo : max(lo, hi - L.band_r);
-            int C = group_chunk(a, sC, splits, lo, hi, scale);
-            cnt += n_chunks(lo, split, C) + n_chunks(split, hi, C);
-        }
-        int tot;
-        block_exclusive_scan(cnt, &tot);
-        if (tot <= L.item_cap || scale >= (1 << 30)) break;
-        scale *= 2;
-    }
     // offsets and items; groups are taken in rounds so the list stays in order
     int base = 0;
     for (int r0 = 0; r0 < nbg; r0 += nthr) {
         const int bg = r0 + threadIdx.x;
-        int cnt = 0, lo = 0, hi = 0, split = 0, C = kMinChunk;
+        int cnt = 0, lo = 0, hi = 0, sp = 0, C = kMinChunk;
         if (bg < nbg) {
-            int b = bg / L.Hkv;
-            hi = __ldcg(&L.kv_len[b]) + 1;
-            lo = __ldcg(&L.grp_lo[bg]);
-            split = a.full_mode ? lo : max(lo, hi - L.band_r);
-            C = group_chunk(a, sC, splits, lo, hi, scale);
-            cnt = n_chunks(lo, split, C) + n_chunks(split, hi, C);
+            group(bg, lo, sp, hi);
+            C = a.plan_mode == 0 ? sC : max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
+            cnt = n_chunks(lo, sp, C) + n_chunks(sp, hi, C);
         }
         int tot;
         const int off = base + block_exclusive_scan(cnt, &tot);
@@ -273,20 +308,24 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
             L.grp_item_off[bg] = off;
             int k = off;
             for (int seg = 0; seg < 2; seg++) {
-                const int s0 = seg == 0 ? lo : split, s1 = seg == 0 ? split : hi;
+                const int s0 = seg == 0 ? lo : sp, s1 = seg == 0 ? sp : hi;
                 if (s1 <= s0) continue;
                 for (int c = s0 / C; c <= (s1 - 1) / C; c++)
-                    L.items[k++] = make_int4(bg, max(s0, c * C), min(s1, (c + 1) * C), seg);
+                    if (k < L.item_cap) L.items[k++] = make_int4(bg, max(s0, c * C), min(s1, (c + 1) * C), seg);
             }
         }
         base += tot;
     }
     if (threadIdx.x == 0) {
+        if (base > L.item_cap) {   // cannot happen with the C chosen above; keep the list in bounds
+            atomicOr(L.err, kErrPos);
+            base = L.item_cap;
+        }
         L.grp_item_off[nbg] = base;
         *L.n_items = base;
         atomicAdd(&L.stats[kStSteps], 1ull);
-        atomicAdd(&L.stats[kStKvRead], (unsigned long long)T);
-        atomicAdd(&L.stats[kStKvFull], (unsigned long long)Tfull);
+        atomicAdd(&L.stats[kStKvRead], (unsigned long long)s_T);
+        atomicAdd(&L.stats[kStKvFull], (unsigned long long)s_Tf);
         atomicAdd(&L.stats[kStItems], (unsigned long long)base);
         if (!a.full_mode) atomicAdd(&L.stats[kStDecisions], (unsigned long long)a.batch * L.H);
         *L.ticket = 0u;   // ready for the next launch
@@ -295,9 +334,13 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
 
 // ---------------------------------------------------------------------------
 // match_plan: grid (Hkv, batch), block G warps (warp w = query head g*G + w).
+// Match (Figure 2(a)): lane e evaluates ring entry e (and e+32), so all the
+// ring's loads are in flight at once; a warp argmin then picks the nearest
+// entry (ties to the larger position).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
 {
+    __shared__ __align__(16) uint4 s_q[32][16];
     const int g = blockIdx.x, b = blockIdx.y;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = L.G, H = L.H;
@@ -326,28 +369,56 @@ __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
 
     int lo_h = 0;
     if (!a.full_mode) {
-        // keep the post-RoPE query for Amend (the caller may reuse its buffer)
-        if (lane < 16)
-            reinterpret_cast<uint4 *>(L.q_stash + bh * kD)[lane] =
-                reinterpret_cast<const uint4 *>(a.q_post + bh * kD)[lane];
-
-        // Match: D_e = ||q~_m - q~_e||^2 over valid entries, fp32, lane owns 4 dims.
-        const float4 q = load_bf16x4(a.q_pre + bh * kD + 4 * lane);
-        const float qn2 = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
+        if (lane < 16) {
+            s_q[w][lane] = reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[lane];
+        } else {   // keep the post-RoPE query for Amend (the caller may reuse its buffer)
+            reinterpret_cast<uint4 *>(L.q_stash + bh * kD)[lane - 16] =
+                reinterpret_cast<const uint4 *>(a.q_post + bh * kD)[lane - 16];
+        }
+        __syncwarp();
+        const float4 q4 = load_bf16x4(reinterpret_cast<const __nv_bfloat16 *>(s_q[w]) + 4 * lane);
+        const float qn2 = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
         const int32_t *rpos = L.ring_pos + (size_t)b * L.ring_len;
         const __nv_bfloat16 *rq = L.ring_q + bh * L.ring_len * kD;
         int best = -1, best_pos = 0;
         float bestD = CUDART_INF_F;
-        for (int e = 0; e < L.ring_len; e++) {
+        for (int e = lane; e < L.ring_len; e += 32) {
             const int pe = rpos[e];
             if (pe <= 0) continue;
-            const float4 c = load_bf16x4(rq + (size_t)e * kD + 4 * lane);
-            const float dx = q.x - c.x, dy = q.y - c.y, dz = q.z - c.z, dw = q.w - c.w;
-            const float De = warp_sum(dx * dx + dy * dy + dz * dz + dw * dw);
+            const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)e * kD);
+            uint4 c[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) c[i] = ent[i];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const uint4 qq = s_q[w][i];
+                const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w}, ca[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[j]));
+                    const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ca[j]));
+                    const float d0 = qf.x - cf.x, d1 = qf.y - cf.y;
+                    acc[j] = fmaf(d0, d0, acc[j]);
+                    acc[j] = fmaf(d1, d1, acc[j]);
+                }
+            }
+            const float De = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             if (best < 0 || De < bestD || (De == bestD && pe > best_pos)) {
                 best = e;
                 bestD = De;
                 best_pos = pe;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float oD = __shfl_xor_sync(0xffffffffu, bestD, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, best, o);
+            const int op = __shfl_xor_sync(0xffffffffu, best_pos, o);
+            if (oe >= 0 && (best < 0 || oD < bestD || (oD == bestD && op > best_pos))) {
+                best = oe;
+                bestD = oD;
+                best_pos = op;
             }
         }
         const int hit = best >= 0 && bestD < L.tau2 * qn2;
@@ -373,25 +444,24 @@ __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
             L.dec_lo[bh] = lo_h;
             if (eff >= 0) atomicAdd(&L.stats[kStHits], 1ull);
         }
-        // Stage q~_m into the slot this step's Amend completes.  Only this
-        // warp reads this head's ring queries before that Amend has run.
+        // Stage q~_m into the slot this step's Amend completes (the old entry's
+        // query has been read above).  Only this warp reads this head's ring
+        // queries before that Amend has run.
         __syncwarp();
-        if (lane < 16)
-            reinterpret_cast<uint4 *>(L.ring_q + (bh * L.ring_len + slot_new) * kD)[lane] =
-                reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[lane];
+        if (lane < 16) reinterpret_cast<uint4 *>(L.ring_q + (bh * L.ring_len + slot_new) * kD)[lane] = s_q[w][lane];
     } else if (lane == 0) {
         L.dec_slot[bh] = -1;
         L.dec_lo[bh] = 0;
     }
 
     // group span start = min over the group's heads; then the ticket
-    __shared__ int s_lo[32];
+    __shared__ int s_glo[32];
     __shared__ int s_last;
-    if (lane == 0) s_lo[w] = lo_h;
+    if (lane == 0) s_glo[w] = lo_h;
     __syncthreads();
     if (threadIdx.x == 0) {
-        int lo = s_lo[0];
-        for (int i = 1; i < G; i++) lo = min(lo, s_lo[i]);
+        int lo = s_glo[0];
+        for (int i = 1; i < G; i++) lo = min(lo, s_glo[i]);
         L.grp_lo[(size_t)b * L.Hkv + g] = lo;
         __threadfence();
         const unsigned t = atomicAdd(L.ticket, 1u);
@@ -621,30 +691,27 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     }
 }
 
-struct Acc {
-    float M, L;
-    float4 O;
-};
-
-__device__ __forceinline__ void acc_add(Acc &A, float M, float Lw, float4 O)
+// ---------------------------------------------------------------------------
+// combine: one warp per (request, head).  Merges the group's item partials --
+// segment 0 (before the amend band) and segment 1 (the band) -- and, on a hit,
+// the ring's AS_{1:p-r} (Figure 2(b), "log-domain merge").  Two passes keep
+// every load independent: per-segment maxima first, then weighted sums.
+// Writes out (bf16), lse_out, and for Amend AS_{1:m}, the direct AS_{1:m-r}
+// and the band summary AS_{m-r+1:m}.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fma4(float4 &acc, float w, float4 v)
 {
-    const float Mn = fmaxf(A.M, M);
-    if (Mn == -CUDART_INF_F) return;
-    const float a = exp2f(A.M - Mn), c = exp2f(M - Mn);
-    A.L = A.L * a + Lw * c;
-    A.O.x = A.O.x * a + O.x * c;
-    A.O.y = A.O.y * a + O.y * c;
-    A.O.z = A.O.z * a + O.z * c;
-    A.O.w = A.O.w * a + O.w * c;
-    A.M = Mn;
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
 }
 
-// ---------------------------------------------------------------------------
-// combine: one warp per (request, head).  Merges the group's item partials
-// (segment 0: before the amend band, segment 1: the band) and, on a hit,
-// the ring's AS_{1:p-r}.  Writes out (bf16), lse_out, AS_{1:m} and the
-// direct AS_{1:m-r} for Amend.
-// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 scale4(float4 v, float s)
+{
+    return make_float4(v.x * s, v.y * s, v.z * s, v.w * s);
+}
+
 __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
 {
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -653,45 +720,75 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
     const int b = gw / L.H, h = gw - b * L.H;
     const int g = h / L.G, hh = h - g * L.G;
     const int bg = b * L.Hkv + g;
-    Acc pre = {-CUDART_INF_F, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-    Acc band = pre;
+    const float NEG = -CUDART_INF_F;
+
+    float m_ring = NEG;
+    float4 o_ring = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!a.full_mode) {
         const int eff = L.dec_slot[gw];
         if (eff >= 0) {
             const size_t e = (size_t)gw * L.ring_len + eff;
             const float lse = L.ring_lse[e];
-            if (lse != -CUDART_INF_F)
-                acc_add(pre, lse * kLog2e, 1.f, *reinterpret_cast<const float4 *>(L.ring_o + e * kD + 4 * lane));
+            if (lse != NEG) {
+                m_ring = lse * kLog2e;
+                o_ring = *reinterpret_cast<const float4 *>(L.ring_o + e * kD + 4 * lane);
+            }
         }
     }
     const int off0 = L.grp_item_off[bg], off1 = L.grp_item_off[bg + 1];
-    for (int i = off0; i < off1; i++) {
-        const int seg = L.items[i].w;
-        const float2 ml = L.part_ml[(size_t)i * L.G + hh];
-        const float4 o = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
-        acc_add(seg ? band : pre, ml.x, ml.y, o);
+    // pass 1: maxima per segment
+    float mp = m_ring, mb = NEG;
+    for (int i = off0 + lane; i < off1; i += 32) {
+        const float mi = L.part_ml[(size_t)i * L.G + hh].x;
+        if (L.items[i].w) mb = fmaxf(mb, mi);
+        else mp = fmaxf(mp, mi);
     }
-    Acc full = pre;
-    acc_add(full, band.M, band.L, band.O);
-    const float inv = 1.f / full.L;
-    const float4 of = make_float4(full.O.x * inv, full.O.y * inv, full.O.z * inv, full.O.w * inv);
-    const float lse = (full.M + log2f(full.L)) * kLn2;
+    mp = warp_max(mp);
+    mb = warp_max(mb);
+    const float bp = mp == NEG ? 0.f : mp, bb = mb == NEG ? 0.f : mb;
+    // pass 2: weighted sums (independent loads; accumulation order is fixed)
+    float lp = 0.f, lb = 0.f;
+    float4 op = make_float4(0.f, 0.f, 0.f, 0.f), ob = op;
+    if (m_ring != NEG) {
+        const float wr = exp2f(m_ring - bp);
+        lp = wr;
+        op = scale4(o_ring, wr);
+    }
+#pragma unroll 4
+    for (int i = off0; i < off1; i++) {
+        const float2 ml = L.part_ml[(size_t)i * L.G + hh];
+        const int seg = L.items[i].w;
+        const float4 o = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
+        const float wi = exp2f(ml.x - (seg ? bb : bp));
+        if (seg) {
+            lb = fmaf(ml.y, wi, lb);
+            fma4(ob, wi, o);
+        } else {
+            lp = fmaf(ml.y, wi, lp);
+            fma4(op, wi, o);
+        }
+    }
+    // AS_{1:m} = pre (+) band
+    const float mf = fmaxf(lp > 0.f ? bp : NEG, lb > 0.f ? bb : NEG);
+    const float wp = lp > 0.f ? exp2f(bp - mf) : 0.f, wb = lb > 0.f ? exp2f(bb - mf) : 0.f;
+    const float lf = lp * wp + lb * wb;
+    float4 of = scale4(op, wp);
+    fma4(of, wb, ob);
+    of = scale4(of, 1.f / lf);
+    const float lse = (mf + log2f(lf)) * kLn2;
     const __nv_bfloat162 lo2 = __floats2bfloat162_rn(of.x, of.y), hi2 = __floats2bfloat162_rn(of.z, of.w);
     *reinterpret_cast<uint2 *>(a.out + (size_t)gw * kD + 4 * lane) = make_uint2(bf16x2_bits(lo2), bf16x2_bits(hi2));
     if (a.lse_out && lane == 0) a.lse_out[gw] = lse;
     if (!a.full_mode) {
         *reinterpret_cast<float4 *>(L.as_full_o + (size_t)gw * kD + 4 * lane) = of;
-        float4 op = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lp = -CUDART_INF_F;
-        if (pre.L > 0.f) {
-            const float ip = 1.f / pre.L;
-            op = make_float4(pre.O.x * ip, pre.O.y * ip, pre.O.z * ip, pre.O.w * ip);
-            lp = (pre.M + log2f(pre.L)) * kLn2;
-        }
-        *reinterpret_cast<float4 *>(L.as_pre_o + (size_t)gw * kD + 4 * lane) = op;
+        *reinterpret_cast<float4 *>(L.as_pre_o + (size_t)gw * kD + 4 * lane) =
+            lp > 0.f ? scale4(op, 1.f / lp) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(L.as_band_o + (size_t)gw * kD + 4 * lane) =
+            lb > 0.f ? scale4(ob, 1.f / lb) : make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane == 0) {
             L.as_full_lse[gw] = lse;
-            L.as_pre_lse[gw] = lp;
+            L.as_pre_lse[gw] = lp > 0.f ? (bp + log2f(lp)) * kLn2 : NEG;
+            L.as_band_lse[gw] = lb > 0.f ? (bb + log2f(lb)) * kLn2 : NEG;
         }
     } else if (h == 0 && lane == 0) {
         L.kv_len[b] = L.m_cur[b];   // the full step has no Amend to commit the length
@@ -699,12 +796,16 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// amend (side stream): grid (Hkv, batch), block G warps.
-// AS_{m-r+1:m} with q_m (band recompute, fp32), AS_{1:m-r} = AS_{1:m} (-)
-// band, ring insert at the step's slot, then commit position and length.
+// amend (side stream, Figure 2(c)): grid (Hkv, batch), block G warps.
+// Rectification term AS_{m-r+1:m} with q_m -- either the band summary
+// Complete produced (amend_band 0) or recomputed here from the KV store
+// through shared-memory tiles (amend_band 1) -- then AS_{1:m-r} =
+// AS_{1:m} (-) band (log-domain removal), ring insert at the step's slot,
+// and finally the step's position and length are committed.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) amend_kernel(Layout L, StepArgs a)
 {
+    extern __shared__ __align__(16) uint8_t band_smem[];   // [kBandTile][kBandRow] K, then V; q per warp
     const int g = blockIdx.x, b = blockIdx.y;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = g * L.G + w;
@@ -712,32 +813,80 @@ __global__ void __launch_bounds__(1024) amend_kernel(Layout L, StepArgs a)
     const int m = L.m_cur[b];
     const int slot = L.slot_cur[b];
     const int r = L.band_r;
+    const float NEG = -CUDART_INF_F;
     float4 oe = make_float4(0.f, 0.f, 0.f, 0.f);
-    float le = -CUDART_INF_F;
+    float le = NEG;
+    bool ok = true;
     if (m > r) {
-        const float4 q = load_bf16x4(L.q_stash + gw * kD + 4 * lane);
-        float M = -CUDART_INF_F, Ls = 0.f;
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        bool ok = true;
-        for (int j = m - r; j < m; j++) {
-            const size_t off = kv_block(L, b, g, j >> 4, ok) + (size_t)(j & 15) * kD + 4 * lane;
-            if (!ok) break;
-            const float4 k = load_bf16x4(L.k_pool + off);
-            const float z = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w) * L.scale_log2;
-            const float4 v = load_bf16x4(L.v_pool + off);
-            const float Mn = fmaxf(M, z);
-            const float al = exp2f(M - Mn), p = exp2f(z - Mn);
-            Ls = Ls * al + p;
-            O.x = O.x * al + p * v.x;
-            O.y = O.y * al + p * v.y;
-            O.z = O.z * al + p * v.z;
-            O.w = O.w * al + p * v.w;
-            M = Mn;
+        float lb;
+        float4 ob;
+        if (L.amend_band == 0) {
+            lb = L.as_band_lse[gw];
+            ob = *reinterpret_cast<const float4 *>(L.as_band_o + gw * kD + 4 * lane);
+        } else {
+            uint8_t *Ks = band_smem, *Vs = band_smem + kBandTile * kBandRow;
+            uint4 *qs = reinterpret_cast<uint4 *>(band_smem + 2 * kBandTile * kBandRow) + w * 16;
+            if (lane < 16) qs[lane] = reinterpret_cast<const uint4 *>(L.q_stash + gw * kD)[lane];
+            float M = NEG, Ls = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int t0 = m - r; t0 < m; t0 += kBandTile) {
+                const int n = min(kBandTile, m - t0);
+                __syncthreads();   // previous tile consumed
+                for (int c = threadIdx.x; c < n * 32; c += blockDim.x) {
+                    const int tok = c >> 5, part = c & 31, isv = part >> 4, ch = part & 15;
+                    bool okc = true;
+                    const int j = t0 + tok;
+                    const size_t off = kv_block(L, b, g, j >> 4, okc) + (size_t)(j & 15) * kD;
+                    if (!okc) {
+                        ok = false;
+                        continue;
+                    }
+                    const uint4 v = reinterpret_cast<const uint4 *>((isv ? L.v_pool : L.k_pool) + off)[ch];
+                    *reinterpret_cast<uint4 *>((isv ? Vs : Ks) + tok * kBandRow + ch * 16) = v;
+                }
+                __syncthreads();
+                // scores: lane owns tokens lane and lane+32 of the tile
+                float z[2];
+#pragma unroll
+                for (int k = 0; k < 2; k++) {
+                    const int tok = lane + 32 * k;
+                    z[k] = NEG;
+                    if (tok < n) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                        for (int i = 0; i < 16; i++) {
+                            const uint4 kk = *reinterpret_cast<const uint4 *>(Ks + tok * kBandRow + i * 16);
+                            const uint4 qq = qs[i];
+                            const uint32_t ka[4] = {kk.x, kk.y, kk.z, kk.w}, qa[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                            for (int jj = 0; jj < 4; jj++) {
+                                const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ka[jj]));
+                                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[jj]));
+                                acc[jj] = fmaf(kf.x, qf.x, acc[jj]);
+                                acc[jj] = fmaf(kf.y, qf.y, acc[jj]);
+                            }
+                        }
+                        z[k] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * L.scale_log2;
+                    }
+                }
+                const float tmax = warp_max(fmaxf(z[0], z[1]));
+                const float Mn = fmaxf(M, tmax);
+                const float al = exp2f(M - Mn);
+                const float p0 = exp2f(z[0] - Mn), p1 = exp2f(z[1] - Mn);
+                Ls = Ls * al + warp_sum(p0 + p1);
+                O = scale4(O, al);
+                for (int tok = 0; tok < n; tok++) {
+                    const float pt = __shfl_sync(0xffffffffu, tok < 32 ? p0 : p1, tok & 31);
+                    fma4(O, pt, load_bf16x4(reinterpret_cast<const __nv_bfloat16 *>(Vs + tok * kBandRow) + 4 * lane));
+                }
+                M = Mn;
+            }
+            lb = (M + log2f(Ls)) * kLn2;
+            ob = scale4(O, 1.f / Ls);
         }
         if (!ok) {
             if (lane == 0) atomicOr(L.err, kErrPage);
         } else {
-            const float lb = (M + log2f(Ls)) * kLn2;
             const float lf = L.as_full_lse[gw];
             const float delta = fminf(lb - lf, 0.f);
             const float cond = -expm1f(delta);   // 1 - e^delta
@@ -746,11 +895,10 @@ __global__ void __launch_bounds__(1024) amend_kernel(Layout L, StepArgs a)
                 le = L.as_pre_lse[gw];
                 if (lane == 0) atomicAdd(&L.stats[kStDirect], 1ull);
             } else {
-                const float wgt = expf(delta);
-                const float inv_ls = 1.f / Ls, inv_c = 1.f / cond;
+                const float wgt = expf(delta), inv_c = 1.f / cond;
                 const float4 of = *reinterpret_cast<const float4 *>(L.as_full_o + gw * kD + 4 * lane);
-                oe = make_float4((of.x - wgt * O.x * inv_ls) * inv_c, (of.y - wgt * O.y * inv_ls) * inv_c,
-                                 (of.z - wgt * O.z * inv_ls) * inv_c, (of.w - wgt * O.w * inv_ls) * inv_c);
+                oe = make_float4((of.x - wgt * ob.x) * inv_c, (of.y - wgt * ob.y) * inv_c,
+                                 (of.z - wgt * ob.z) * inv_c, (of.w - wgt * ob.w) * inv_c);
                 le = lf + log1mexp_f(delta);
             }
         }
@@ -835,9 +983,18 @@ cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
     return cudaGetLastError();
 }
 
+static size_t amend_smem(int G) { return (size_t)2 * kBandTile * kBandRow + (size_t)G * kD * 2; }
+
+cudaError_t amend_kernel_config()
+{
+    return cudaFuncSetAttribute(amend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)amend_smem(kMaxGroup));
+}
+
 cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    amend_kernel<<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
+    const size_t smem = L.amend_band ? amend_smem(L.G) : 0;
+    amend_kernel<<<dim3(L.Hkv, a.batch), L.G * 32, smem, s>>>(L, a);
     return cudaGetLastError();
 }
 

@@ -39,14 +39,15 @@ def check_out(out, lse, ref, what=""):
 class Pair:
     """A MAC handle and the oracle over identical inputs."""
 
-    def __init__(self, cfg: W.DecodeConfig, contexts=None, page_size=16, plan_mode=0, extra_steps=0):
+    def __init__(self, cfg: W.DecodeConfig, contexts=None, page_size=16, plan_mode=0, extra_steps=0, amend_band=0):
         self.cfg = cfg
         B = cfg.batch
         self.contexts = list(contexts) if contexts is not None else [cfg.context] * B
         self.t_max = max(self.contexts) + cfg.steps + extra_steps
         K, V = W.prefill_kv(cfg) if cfg.context > 0 else (None, None)
         self.mac = MacAttention(cfg.heads, cfg.kv_heads, cfg.head_dim, cfg.ring_len, cfg.band_r, cfg.tau,
-                                max_batch=B, max_ctx=self.t_max, page_size=page_size, plan_mode=plan_mode)
+                                max_batch=B, max_ctx=self.t_max, page_size=page_size, plan_mode=plan_mode,
+                                amend_band=amend_band)
         if page_size:
             ppr = (self.t_max + 15) // 16
             self.pages = W.page_tables(B, ppr, seed=cfg.seed).cuda()

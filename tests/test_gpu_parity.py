@@ -47,10 +47,11 @@ def test_full_step_every_group_size(kv_heads):
         p.full_step(t)
 
 
+@pytest.mark.parametrize("amend_band", [0, 1])
 @pytest.mark.parametrize("page_size", [16, 0])
-@pytest.mark.parametrize("band_r,ring_len", [(32, 8), (64, 16), (16, 1)])
-def test_mac_chain_under_oracle_decisions(page_size, band_r, ring_len):
-    p = _pair(cfg(band_r=band_r, ring_len=ring_len, steps=16), page_size=page_size)
+@pytest.mark.parametrize("band_r,ring_len", [(32, 8), (64, 16), (16, 1), (150, 4)])
+def test_mac_chain_under_oracle_decisions(page_size, band_r, ring_len, amend_band):
+    p = _pair(cfg(band_r=band_r, ring_len=ring_len, steps=16), page_size=page_size, amend_band=amend_band)
     hits = 0
     for t in range(16):
         ref, _ = p.mac_step(t, force=True)
@@ -71,9 +72,10 @@ def test_mac_chain_own_decisions():
     assert st["hits"] == hits and st["head_decisions"] == 16 * 2 * 32
 
 
+@pytest.mark.parametrize("amend_band", [0, 1])
 @pytest.mark.parametrize("kv_heads", [32, 8, 4, 1])
-def test_mac_chain_group_sizes(kv_heads):
-    p = _pair(cfg(kv_heads=kv_heads, context=500, steps=10, rho=0.995, ring_len=4))
+def test_mac_chain_group_sizes(kv_heads, amend_band):
+    p = _pair(cfg(kv_heads=kv_heads, context=500, steps=10, rho=0.995, ring_len=4), amend_band=amend_band)
     for t in range(10):
         p.mac_step(t, force=True)
 
@@ -85,8 +87,9 @@ def test_heterogeneous_rho_and_lengths():
         p.mac_step(t, force=True)
 
 
-def test_empty_prefill_and_band_wider_than_context():
-    p = _pair(cfg(context=0, steps=20, band_r=64, ring_len=4, rho=0.999))
+@pytest.mark.parametrize("amend_band", [0, 1])
+def test_empty_prefill_and_band_wider_than_context(amend_band):
+    p = _pair(cfg(context=0, steps=20, band_r=64, ring_len=4, rho=0.999), amend_band=amend_band)
     for t in range(20):
         p.mac_step(t, force=True)
 
@@ -145,3 +148,15 @@ def test_reset_request_restarts_cleanly():
     p.mac.sync()
     r = p.mac.read_ring(0)
     assert r["kv_len"] == 0 and r["steps"] == 0 and not r["pos"].any()
+
+
+def test_plan_fits_one_wave_of_the_grid():
+    """Balanced planning keeps the work list within the persistent grid when
+    there are few segments, so no CTA runs a second item."""
+    c = cfg(batch=1, context=20000, steps=3, rho=0.5)
+    p = _pair(c)
+    for t in range(3):
+        p.mac_step(t, force=True, check_ring=False)
+    st = p.mac.stats()
+    grid = torch.cuda.get_device_properties(0).multi_processor_count * 2
+    assert st["work_items"] / st["steps"] <= grid
