@@ -235,7 +235,7 @@ def bench_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K_steps, W_steps = args.steps, args.warmup
-    total_steps = W_steps + 2 * K_steps + 2
+    total_steps = W_steps + 3 * K_steps + 2
     cfg = workload(args.workload, args.band_r, total_steps)
     B, H, Hkv, G = cfg.batch, cfg.heads, cfg.kv_heads, cfg.group
 
@@ -263,7 +263,6 @@ def bench_ours(args, ws, rank, local):
     mac.sync()
     torch.cuda.synchronize()
     mac.reset_stats()
-    mac.set_profiling(True)
 
     # timed region: K steps, device events on the launching stream
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -278,16 +277,28 @@ def bench_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         barrier(ws)
     ms = e0.elapsed_time(e1)
-    prof = mac.profile()
-    mac.set_profiling(False)
     st = mac.stats()
     clk = clocks.summary()
     ms_max = max_over_ranks(ms, ws, dev)
     us_step = ms_max * 1e3 / K_steps
 
+    # per-kernel durations: the next K steps again with CUDA events around
+    # every launch (on the stream each kernel runs on); these events sit
+    # between the kernels, so this pass is kept out of the headline time
+    mac.reset_stats()
+    mac.set_profiling(True)
+    for t in range(W_steps + K_steps, W_steps + 2 * K_steps):
+        mac.decode_step(*step_args(t), out=out, lse=lse)
+    mac.join()
+    torch.cuda.synchronize()
+    prof = mac.profile()
+    mac.set_profiling(False)
+    st_p = mac.stats()
+
     # end to end through the C ABI with host (pinned) buffers
     pin = lambda x: x.cpu().pin_memory()
-    h_in = {k: pin(inp[k][W_steps + K_steps:W_steps + 2 * K_steps]) for k in ("q_pre", "q_post", "k_new", "v_new")}
+    e2e_first = W_steps + 2 * K_steps
+    h_in = {k: pin(inp[k][e2e_first:e2e_first + K_steps]) for k in ("q_pre", "q_post", "k_new", "v_new")}
     d_in = [torch.empty_like(inp[k][0]) for k in ("q_pre", "q_post", "k_new", "v_new")]
     h_out = torch.empty((B, H, cfg.head_dim), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
@@ -314,7 +325,9 @@ def bench_ours(args, ws, rank, local):
     steps = st["steps"]
     items = st["work_items"]
     partial = items * G * (128 * 4 + 8)
-    attn_bytes = kv_read + steps * B * H * 256 + partial
+    # the attention kernel's bytes over the profiled pass
+    attn_bytes = (st_p["kv_tokens_read"] * BYTES_PER_KV_TOKEN + st_p["steps"] * B * H * 256
+                  + st_p["work_items"] * G * (128 * 4 + 8))
     L = cfg.ring_len
     ring = steps * B * H * L * 256 + st["hits"] * (128 * 4 + 4)
     io = steps * (B * H * 256 * 2 + B * Hkv * 512 + B * H * 256 + B * H * 4) + 2 * partial
@@ -325,7 +338,7 @@ def bench_ours(args, ws, rank, local):
     peak, peak_kind = measured_peaks()
     achieved = attn_bytes / attn_s / 1e9 if attn_s > 0 else None
     traffic = profiled_traffic(os.path.join(ROOT, "kv_cache_computation_gb300", "csrc", "mac_kernels.cu"))
-    launches = prof["steps"] or steps
+    launches = prof["steps"] or st_p["steps"]
 
     result = {
         "metric": METRIC, "value": round(us_step, 3), "unit": "us/step", "n_gpus": ws, "steps": K_steps,
@@ -351,6 +364,8 @@ def bench_ours(args, ws, rank, local):
                      else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": round(attn_bytes / launches),
                      "avg_launch_us": round(attn_s / launches * 1e6, 3),
+                     "timing": "CUDA events around each attention launch over a second pass of K steps "
+                               "(events between kernels disable launch overlap, so that pass is not the headline)",
                      "traffic": traffic},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},

@@ -259,6 +259,10 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
 
     cudaEvent_t *pe = nullptr;
     if (h->prof && h->prof_steps < kProfCap) pe = &h->prof_ev[h->prof_steps++ * 6];
+    // Programmatic dependent launch overlaps each launch with its
+    // predecessor's tail; event records between the kernels (profiling)
+    // would sit between them, so it is used only when not profiling.
+    a.pdl = pe ? 0 : 1;
 
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[0], s));
     MAC_CUDA(h, launch_match_plan(h->lay, a, s));

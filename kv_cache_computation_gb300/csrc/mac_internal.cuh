@@ -93,6 +93,7 @@ struct StepArgs {
     int full_mode;    // full attention, no Match / Amend
     int grid_ctas;    // attention CTAs
     int plan_mode;    // 0 balanced, 1 equal split per group
+    int pdl;          // launch attention / combine as programmatic dependents
 };
 
 // launchers (mac_kernels.cu)

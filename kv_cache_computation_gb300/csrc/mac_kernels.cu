@@ -66,6 +66,12 @@ __device__ __forceinline__ size_t kv_block(const Layout &L, int b, int g, int pg
     return (((size_t)b * L.Hkv + g) * L.ctx_stride + (size_t)pg * kPage) * kD;
 }
 
+// Programmatic dependent launch: a dependent grid may start while its
+// predecessor in the stream still runs; it waits here until the predecessor
+// has completed and its memory is visible.  Both are no-ops in a plain launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -341,6 +347,7 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
 __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
 {
     __shared__ __align__(16) uint4 s_q[32][16];
+    pdl_launch_dependents();
     const int g = blockIdx.x, b = blockIdx.y;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = L.G, H = L.H;
@@ -348,27 +355,22 @@ __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
     const size_t bh = (size_t)b * H + h;
     const int kvlen = L.kv_len[b];
     const int m = kvlen + 1;            // 1-based position of the new token (index kvlen)
-
-    // KV append of the new token: warp 0 moves K (lanes 0-15) and V (16-31).
-    if (w == 0) {
-        bool ok = true;
-        const size_t off = kv_block(L, b, g, kvlen >> 4, ok);
-        if (ok) {
-            const __nv_bfloat16 *src = (lane < 16 ? a.k_new : a.v_new) + ((size_t)b * L.Hkv + g) * kD;
-            __nv_bfloat16 *dst = (lane < 16 ? L.k_pool : L.v_pool) + off + (size_t)(kvlen & 15) * kD;
-            reinterpret_cast<uint4 *>(dst)[lane & 15] = reinterpret_cast<const uint4 *>(src)[lane & 15];
-        } else if (lane == 0) {
-            atomicOr(L.err, kErrPage);
-        }
-    }
     const int slot_new = a.full_mode ? 0 : L.step_ctr[b] % L.ring_len;
-    if (g == 0 && threadIdx.x == 0) {
-        L.m_cur[b] = m;
-        L.slot_cur[b] = slot_new;
-    }
 
     int lo_h = 0;
     if (!a.full_mode) {
+        const int32_t *rpos = L.ring_pos + (size_t)b * L.ring_len;
+        const __nv_bfloat16 *rq = L.ring_q + bh * L.ring_len * kD;
+        // Every load that depends on nothing is issued first: entry `lane`
+        // of the ring (position and query) and this head's queries.
+        int pe0 = 0;
+        uint4 c[16];
+        if (lane < L.ring_len) {
+            pe0 = rpos[lane];
+            const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)lane * kD);
+#pragma unroll
+            for (int i = 0; i < 16; i++) c[i] = ent[i];
+        }
         if (lane < 16) {
             s_q[w][lane] = reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[lane];
         } else {   // keep the post-RoPE query for Amend (the caller may reuse its buffer)
@@ -378,22 +380,13 @@ __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
         __syncwarp();
         const float4 q4 = load_bf16x4(reinterpret_cast<const __nv_bfloat16 *>(s_q[w]) + 4 * lane);
         const float qn2 = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
-        const int32_t *rpos = L.ring_pos + (size_t)b * L.ring_len;
-        const __nv_bfloat16 *rq = L.ring_q + bh * L.ring_len * kD;
-        int best = -1, best_pos = 0;
-        float bestD = CUDART_INF_F;
-        for (int e = lane; e < L.ring_len; e += 32) {
-            const int pe = rpos[e];
-            if (pe <= 0) continue;
-            const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)e * kD);
-            uint4 c[16];
-#pragma unroll
-            for (int i = 0; i < 16; i++) c[i] = ent[i];
+        // D_e = ||q~_m - q~_e||^2 in fp32 for the entries this lane owns
+        auto dist = [&](const uint4 (&cc)[16]) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 16; i++) {
                 const uint4 qq = s_q[w][i];
-                const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w}, ca[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
+                const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w}, ca[4] = {cc[i].x, cc[i].y, cc[i].z, cc[i].w};
 #pragma unroll
                 for (int j = 0; j < 4; j++) {
                     const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[j]));
@@ -403,7 +396,22 @@ __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
                     acc[j] = fmaf(d1, d1, acc[j]);
                 }
             }
-            const float De = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        };
+        int best = -1, best_pos = 0;
+        float bestD = CUDART_INF_F;
+        if (pe0 > 0) {
+            best = lane;
+            bestD = dist(c);
+            best_pos = pe0;
+        }
+        for (int e = lane + 32; e < L.ring_len; e += 32) {   // rings longer than a warp
+            const int pe = rpos[e];
+            if (pe <= 0) continue;
+            const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)e * kD);
+#pragma unroll
+            for (int i = 0; i < 16; i++) c[i] = ent[i];
+            const float De = dist(c);
             if (best < 0 || De < bestD || (De == bestD && pe > best_pos)) {
                 best = e;
                 bestD = De;
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
         int p = 0;
         if (eff >= L.ring_len) eff = -2;
         if (eff >= 0) {
-            p = rpos[eff];
+            p = eff == best ? best_pos : rpos[eff];
             if (p <= 0 || p >= m) eff = -2;
         }
         if (eff == -2) {   // a forced slot that holds no entry: treat as a miss, flag it
@@ -452,6 +460,23 @@ __global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
     } else if (lane == 0) {
         L.dec_slot[bh] = -1;
         L.dec_lo[bh] = 0;
+    }
+
+    // KV append of the new token: warp 0 moves K (lanes 0-15) and V (16-31).
+    if (w == 0) {
+        bool ok = true;
+        const size_t off = kv_block(L, b, g, kvlen >> 4, ok);
+        if (ok) {
+            const __nv_bfloat16 *src = (lane < 16 ? a.k_new : a.v_new) + ((size_t)b * L.Hkv + g) * kD;
+            __nv_bfloat16 *dst = (lane < 16 ? L.k_pool : L.v_pool) + off + (size_t)(kvlen & 15) * kD;
+            reinterpret_cast<uint4 *>(dst)[lane & 15] = reinterpret_cast<const uint4 *>(src)[lane & 15];
+        } else if (lane == 0) {
+            atomicOr(L.err, kErrPage);
+        }
+    }
+    if (g == 0 && threadIdx.x == 0) {
+        L.m_cur[b] = m;
+        L.slot_cur[b] = slot_new;
     }
 
     // group span start = min over the group's heads; then the ticket
@@ -499,6 +524,8 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     const int gtid = threadIdx.x - pl * gthreads;
     uint8_t *lane_smem = smem + (size_t)pl * S * kStageBytes;
     const int r4 = lane >> 2, c4 = lane & 3;
+    pdl_launch_dependents();
+    pdl_wait();   // the work list comes from match_plan
     const int n_items = *L.n_items;
     const float sl2 = L.scale_log2;
 
@@ -721,6 +748,7 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
     const int g = h / L.G, hh = h - g * L.G;
     const int bg = b * L.Hkv + g;
     const float NEG = -CUDART_INF_F;
+    pdl_wait();   // partials come from the attention kernel
 
     float m_ring = NEG;
     float4 o_ring = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -746,7 +774,8 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
     mp = warp_max(mp);
     mb = warp_max(mb);
     const float bp = mp == NEG ? 0.f : mp, bb = mb == NEG ? 0.f : mb;
-    // pass 2: weighted sums (independent loads; accumulation order is fixed)
+    // pass 2: weighted sums.  Loads are issued in batches of 8 independent
+    // items before any is used; the accumulation order stays fixed.
     float lp = 0.f, lb = 0.f;
     float4 op = make_float4(0.f, 0.f, 0.f, 0.f), ob = op;
     if (m_ring != NEG) {
@@ -754,18 +783,29 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
         lp = wr;
         op = scale4(o_ring, wr);
     }
-#pragma unroll 4
-    for (int i = off0; i < off1; i++) {
-        const float2 ml = L.part_ml[(size_t)i * L.G + hh];
-        const int seg = L.items[i].w;
-        const float4 o = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
-        const float wi = exp2f(ml.x - (seg ? bb : bp));
-        if (seg) {
-            lb = fmaf(ml.y, wi, lb);
-            fma4(ob, wi, o);
-        } else {
-            lp = fmaf(ml.y, wi, lp);
-            fma4(op, wi, o);
+    constexpr int kBatch = 8;
+    for (int i0 = off0; i0 < off1; i0 += kBatch) {
+        float2 ml[kBatch];
+        int sg[kBatch];
+        float4 ov[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; k++) {
+            const int i = min(i0 + k, off1 - 1);
+            ml[k] = L.part_ml[(size_t)i * L.G + hh];
+            sg[k] = L.items[i].w;
+            ov[k] = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; k++) {
+            if (i0 + k >= off1) break;
+            const float wi = exp2f(ml[k].x - (sg[k] ? bb : bp));
+            if (sg[k]) {
+                lb = fmaf(ml[k].y, wi, lb);
+                fma4(ob, wi, ov[k]);
+            } else {
+                lp = fmaf(ml[k].y, wi, lp);
+                fma4(op, wi, ov[k]);
+            }
         }
     }
     // AS_{1:m} = pre (+) band
@@ -970,17 +1010,33 @@ cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s
     return cudaGetLastError();
 }
 
+template <typename Kernel>
+static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                    const Layout &L, const StepArgs &a)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, L, a);
+}
+
 cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)
 {
-    attention_kernel<kAttnWarps, kAttnStages><<<a.grid_ctas, kAttnWarps * 32, smem, s>>>(L, a);
-    return cudaGetLastError();
+    return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages>, dim3(a.grid_ctas), dim3(kAttnWarps * 32), smem,
+                            s, a.pdl != 0, L, a);
 }
 
 cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
     const int warps = a.batch * L.H;
-    combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(L, a);
-    return cudaGetLastError();
+    return launch_maybe_pdl(combine_kernel, dim3((warps + 3) / 4), dim3(128), 0, s, a.pdl != 0, L, a);
 }
 
 static size_t amend_smem(int G) { return (size_t)2 * kBandTile * kBandRow + (size_t)G * kD * 2; }
