@@ -47,7 +47,7 @@ struct Sizes {
     size_t r_pos, r_q, r_o, r_lse;
     size_t s_page, s_kvlen, s_step, s_mcur, s_slot, s_own_slot, s_own_hit, s_dslot, s_dlo, s_dD, s_dqn2,
         s_forced, s_qstash, s_glo, s_goff, s_items, s_nitems, s_ticket, s_po, s_pml, s_afo, s_afl, s_apo,
-        s_apl, s_abo, s_abl, s_stats, s_err;
+        s_apl, s_stats, s_err;
 };
 
 bool valid_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16 || G == 32; }
@@ -119,8 +119,6 @@ mac_status compute_sizes(const mac_config *c, Sizes *z)
     z->s_afl = s.take(BH * 4);
     z->s_apo = s.take(BH * kD * 4);
     z->s_apl = s.take(BH * 4);
-    z->s_abo = s.take(BH * kD * 4);
-    z->s_abl = s.take(BH * 4);
     z->s_stats = s.take(kStCount * 8);
     z->s_err = s.take(4);
     z->scratch = s.off;
@@ -271,7 +269,8 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[2], s));
     MAC_CUDA(h, launch_combine(h->lay, a, s));
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[3], s));
-    if (!full) {
+    if (!full && h->cfg.amend_band == 1) {
+        // Amend recomputes the band: its own kernel on the side stream
         MAC_CUDA(h, cudaEventRecord(h->ev_complete, s));
         MAC_CUDA(h, cudaStreamWaitEvent(h->side, h->ev_complete, 0));
         if (pe) MAC_CUDA(h, cudaEventRecord(pe[4], h->side));
@@ -280,7 +279,8 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
         MAC_CUDA(h, cudaEventRecord(h->ev_amend, h->side));
         h->amend_pending = true;
     } else if (pe) {
-        // a full step has no Amend: an empty interval on the main stream
+        // Amend ran in the combine epilogue (or a full step has none): an
+        // empty interval on the main stream
         MAC_CUDA(h, cudaEventRecord(pe[4], s));
         MAC_CUDA(h, cudaEventRecord(pe[5], s));
     }
@@ -414,8 +414,6 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     L.as_full_lse = (float *)(sc + z.s_afl);
     L.as_pre_o = (float *)(sc + z.s_apo);
     L.as_pre_lse = (float *)(sc + z.s_apl);
-    L.as_band_o = (float *)(sc + z.s_abo);
-    L.as_band_lse = (float *)(sc + z.s_abl);
     L.amend_band = cfg->amend_band;
     L.stats = (unsigned long long *)(sc + z.s_stats);
     L.err = (uint32_t *)(sc + z.s_err);

@@ -78,7 +78,6 @@ struct Layout {
     // merged summaries kept for Amend
     float *as_full_o, *as_full_lse;   // AS_{1:m}
     float *as_pre_o, *as_pre_lse;     // AS_{1:m-r} formed directly (fallback of the removal)
-    float *as_band_o, *as_band_lse;   // AS_{m-r+1:m} from Complete's band segment
 
     unsigned long long *stats;        // [kStCount]
     uint32_t *err;

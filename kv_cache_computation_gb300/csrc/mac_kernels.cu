@@ -344,7 +344,8 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
 // ring's loads are in flight at once; a warp argmin then picks the nearest
 // entry (ties to the larger position).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) match_plan_kernel(Layout L, StepArgs a)
+template <int MAX_THREADS>
+__global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepArgs a)
 {
     __shared__ __align__(16) uint4 s_q[32][16];
     pdl_launch_dependents();
@@ -719,13 +720,20 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 }
 
 // ---------------------------------------------------------------------------
-// combine: one warp per (request, head).  Merges the group's item partials --
-// segment 0 (before the amend band) and segment 1 (the band) -- and, on a hit,
-// the ring's AS_{1:p-r} (Figure 2(b), "log-domain merge").  Two passes keep
-// every load independent: per-segment maxima first, then weighted sums.
-// Writes out (bf16), lse_out, and for Amend AS_{1:m}, the direct AS_{1:m-r}
-// and the band summary AS_{m-r+1:m}.
+// combine: one block of kCombineWarps warps per (request, head).  Merges the
+// group's item partials -- segment 0 (before the amend band) and segment 1
+// (the band) -- and, on a hit, the ring's AS_{1:p-r} (Figure 2(b),
+// "log-domain merge").  Items are spread over the warps so every load is in
+// flight at once: block-wide maxima per segment first, then each warp's
+// weighted sums, then a shared-memory reduction.
+//
+// Epilogue: out (bf16) and lse_out; then, with amend_band 0, Amend itself
+// (Figure 2(c)): the band segment is the rectification term AS_{m-r+1:m},
+// AS_{1:m-r} = AS_{1:m} (-) band, and the ring insert.  With amend_band 1 the
+// summaries are handed to the side-stream Amend kernel instead.
 // ---------------------------------------------------------------------------
+constexpr int kCombineWarps = 8;
+
 __device__ __forceinline__ void fma4(float4 &acc, float w, float4 v)
 {
     acc.x = fmaf(w, v.x, acc.x);
@@ -739,11 +747,33 @@ __device__ __forceinline__ float4 scale4(float4 v, float s)
     return make_float4(v.x * s, v.y * s, v.z * s, v.w * s);
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
+// AS_{1:m-r} from AS_{1:m} and the band AS_{m-r+1:m} (natural-log lse) by
+// log-domain removal; the direct form `pre` when 1 - e^delta is too small
+// for fp32.  Returns whether the direct form was taken.
+__device__ __forceinline__ bool remove_band(float lf, float4 of, float lb, float4 ob, float lpre, float4 opre,
+                                            float &le, float4 &oe)
 {
-    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= a.batch * L.H) return;
+    const float delta = fminf(lb - lf, 0.f);
+    const float cond = -expm1f(delta);   // 1 - e^delta
+    if (cond < kRemovalMinCond) {
+        le = lpre;
+        oe = opre;
+        return true;
+    }
+    const float wgt = expf(delta), inv_c = 1.f / cond;
+    oe = make_float4((of.x - wgt * ob.x) * inv_c, (of.y - wgt * ob.y) * inv_c, (of.z - wgt * ob.z) * inv_c,
+                     (of.w - wgt * ob.w) * inv_c);
+    le = lf + log1mexp_f(delta);
+    return false;
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, StepArgs a)
+{
+    __shared__ float s_red[2][kCombineWarps];
+    __shared__ float s_l[2][kCombineWarps];
+    __shared__ float4 s_o[2][kCombineWarps][32];
+    const int gw = blockIdx.x;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = gw / L.H, h = gw - b * L.H;
     const int g = h / L.G, hh = h - g * L.G;
     const int bg = b * L.Hkv + g;
@@ -764,40 +794,51 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
         }
     }
     const int off0 = L.grp_item_off[bg], off1 = L.grp_item_off[bg + 1];
-    // pass 1: maxima per segment
+    // block-wide maxima per segment
     float mp = m_ring, mb = NEG;
-    for (int i = off0 + lane; i < off1; i += 32) {
+    for (int i = off0 + threadIdx.x; i < off1; i += blockDim.x) {
         const float mi = L.part_ml[(size_t)i * L.G + hh].x;
         if (L.items[i].w) mb = fmaxf(mb, mi);
         else mp = fmaxf(mp, mi);
     }
     mp = warp_max(mp);
     mb = warp_max(mb);
+    if (lane == 0) {
+        s_red[0][w] = mp;
+        s_red[1][w] = mb;
+    }
+    __syncthreads();
+    mp = s_red[0][0];
+    mb = s_red[1][0];
+#pragma unroll
+    for (int i = 1; i < kCombineWarps; i++) {
+        mp = fmaxf(mp, s_red[0][i]);
+        mb = fmaxf(mb, s_red[1][i]);
+    }
     const float bp = mp == NEG ? 0.f : mp, bb = mb == NEG ? 0.f : mb;
-    // pass 2: weighted sums.  Loads are issued in batches of 8 independent
-    // items before any is used; the accumulation order stays fixed.
+    // each warp's weighted sums over items w, w + kCombineWarps, ...
     float lp = 0.f, lb = 0.f;
     float4 op = make_float4(0.f, 0.f, 0.f, 0.f), ob = op;
-    if (m_ring != NEG) {
+    if (w == 0 && m_ring != NEG) {
         const float wr = exp2f(m_ring - bp);
         lp = wr;
         op = scale4(o_ring, wr);
     }
-    constexpr int kBatch = 8;
-    for (int i0 = off0; i0 < off1; i0 += kBatch) {
+    constexpr int kBatch = 4;
+    for (int i0 = off0 + w; i0 < off1; i0 += kBatch * kCombineWarps) {
         float2 ml[kBatch];
         int sg[kBatch];
         float4 ov[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; k++) {
-            const int i = min(i0 + k, off1 - 1);
+            const int i = min(i0 + k * kCombineWarps, off1 - 1);
             ml[k] = L.part_ml[(size_t)i * L.G + hh];
             sg[k] = L.items[i].w;
             ov[k] = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
         }
 #pragma unroll
         for (int k = 0; k < kBatch; k++) {
-            if (i0 + k >= off1) break;
+            if (i0 + k * kCombineWarps >= off1) break;
             const float wi = exp2f(ml[k].x - (sg[k] ? bb : bp));
             if (sg[k]) {
                 lb = fmaf(ml[k].y, wi, lb);
@@ -807,6 +848,27 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
                 fma4(op, wi, ov[k]);
             }
         }
+    }
+    __syncthreads();   // s_red reused
+    if (lane == 0) {
+        s_l[0][w] = lp;
+        s_l[1][w] = lb;
+    }
+    s_o[0][w][lane] = op;
+    s_o[1][w][lane] = ob;
+    __syncthreads();
+    if (w != 0) return;
+    lp = s_l[0][0];
+    lb = s_l[1][0];
+    op = s_o[0][0][lane];
+    ob = s_o[1][0][lane];
+#pragma unroll
+    for (int i = 1; i < kCombineWarps; i++) {
+        lp += s_l[0][i];
+        lb += s_l[1][i];
+        const float4 x = s_o[0][i][lane], y = s_o[1][i][lane];
+        op.x += x.x; op.y += x.y; op.z += x.z; op.w += x.w;
+        ob.x += y.x; ob.y += y.y; ob.z += y.z; ob.w += y.w;
     }
     // AS_{1:m} = pre (+) band
     const float mf = fmaxf(lp > 0.f ? bp : NEG, lb > 0.f ? bb : NEG);
@@ -819,19 +881,40 @@ __global__ void __launch_bounds__(128) combine_kernel(Layout L, StepArgs a)
     const __nv_bfloat162 lo2 = __floats2bfloat162_rn(of.x, of.y), hi2 = __floats2bfloat162_rn(of.z, of.w);
     *reinterpret_cast<uint2 *>(a.out + (size_t)gw * kD + 4 * lane) = make_uint2(bf16x2_bits(lo2), bf16x2_bits(hi2));
     if (a.lse_out && lane == 0) a.lse_out[gw] = lse;
-    if (!a.full_mode) {
+    if (a.full_mode) {
+        if (h == 0 && lane == 0) L.kv_len[b] = L.m_cur[b];   // the full step has no Amend to commit the length
+        return;
+    }
+    const float4 opre = lp > 0.f ? scale4(op, 1.f / lp) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float lpre = lp > 0.f ? (bp + log2f(lp)) * kLn2 : NEG;
+    if (L.amend_band == 1) {   // the side-stream Amend kernel recomputes the band
         *reinterpret_cast<float4 *>(L.as_full_o + (size_t)gw * kD + 4 * lane) = of;
-        *reinterpret_cast<float4 *>(L.as_pre_o + (size_t)gw * kD + 4 * lane) =
-            lp > 0.f ? scale4(op, 1.f / lp) : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(L.as_band_o + (size_t)gw * kD + 4 * lane) =
-            lb > 0.f ? scale4(ob, 1.f / lb) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(L.as_pre_o + (size_t)gw * kD + 4 * lane) = opre;
         if (lane == 0) {
             L.as_full_lse[gw] = lse;
-            L.as_pre_lse[gw] = lp > 0.f ? (bp + log2f(lp)) * kLn2 : NEG;
-            L.as_band_lse[gw] = lb > 0.f ? (bb + log2f(lb)) * kLn2 : NEG;
+            L.as_pre_lse[gw] = lpre;
         }
-    } else if (h == 0 && lane == 0) {
-        L.kv_len[b] = L.m_cur[b];   // the full step has no Amend to commit the length
+        return;
+    }
+    // Amend in the epilogue: the band segment is AS_{m-r+1:m}(q_m)
+    const int m = L.m_cur[b], slot = L.slot_cur[b];
+    float le = NEG;
+    float4 oe = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m > L.band_r) {
+        const float4 oband = scale4(ob, 1.f / lb);
+        const float lband = (bb + log2f(lb)) * kLn2;
+        if (remove_band(lse, of, lband, oband, lpre, opre, le, oe) && lane == 0)
+            atomicAdd(&L.stats[kStDirect], 1ull);
+    }
+    const size_t e = (size_t)gw * L.ring_len + slot;   // the matched entry was read above
+    *reinterpret_cast<float4 *>(L.ring_o + e * kD + 4 * lane) = oe;
+    if (lane == 0) {
+        L.ring_lse[e] = le;
+        if (h == 0) {   // nothing in this kernel reads these per-request words
+            L.ring_pos[(size_t)b * L.ring_len + slot] = m;
+            L.kv_len[b] = m;
+            L.step_ctr[b] = L.step_ctr[b] + 1;
+        }
     }
 }
 
@@ -856,91 +939,74 @@ __global__ void __launch_bounds__(1024) amend_kernel(Layout L, StepArgs a)
     const float NEG = -CUDART_INF_F;
     float4 oe = make_float4(0.f, 0.f, 0.f, 0.f);
     float le = NEG;
-    bool ok = true;
     if (m > r) {
-        float lb;
-        float4 ob;
-        if (L.amend_band == 0) {
-            lb = L.as_band_lse[gw];
-            ob = *reinterpret_cast<const float4 *>(L.as_band_o + gw * kD + 4 * lane);
-        } else {
-            uint8_t *Ks = band_smem, *Vs = band_smem + kBandTile * kBandRow;
-            uint4 *qs = reinterpret_cast<uint4 *>(band_smem + 2 * kBandTile * kBandRow) + w * 16;
-            if (lane < 16) qs[lane] = reinterpret_cast<const uint4 *>(L.q_stash + gw * kD)[lane];
-            float M = NEG, Ls = 0.f;
-            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int t0 = m - r; t0 < m; t0 += kBandTile) {
-                const int n = min(kBandTile, m - t0);
-                __syncthreads();   // previous tile consumed
-                for (int c = threadIdx.x; c < n * 32; c += blockDim.x) {
-                    const int tok = c >> 5, part = c & 31, isv = part >> 4, ch = part & 15;
-                    bool okc = true;
-                    const int j = t0 + tok;
-                    const size_t off = kv_block(L, b, g, j >> 4, okc) + (size_t)(j & 15) * kD;
-                    if (!okc) {
-                        ok = false;
-                        continue;
-                    }
-                    const uint4 v = reinterpret_cast<const uint4 *>((isv ? L.v_pool : L.k_pool) + off)[ch];
-                    *reinterpret_cast<uint4 *>((isv ? Vs : Ks) + tok * kBandRow + ch * 16) = v;
+        uint8_t *Ks = band_smem, *Vs = band_smem + kBandTile * kBandRow;
+        uint4 *qs = reinterpret_cast<uint4 *>(band_smem + 2 * kBandTile * kBandRow) + w * 16;
+        if (lane < 16) qs[lane] = reinterpret_cast<const uint4 *>(L.q_stash + gw * kD)[lane];
+        bool ok = true;
+        float M = NEG, Ls = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int t0 = m - r; t0 < m; t0 += kBandTile) {
+            const int n = min(kBandTile, m - t0);
+            __syncthreads();   // previous tile consumed
+            for (int c = threadIdx.x; c < n * 32; c += blockDim.x) {
+                const int tok = c >> 5, part = c & 31, isv = part >> 4, ch = part & 15;
+                bool okc = true;
+                const int j = t0 + tok;
+                const size_t off = kv_block(L, b, g, j >> 4, okc) + (size_t)(j & 15) * kD;
+                if (!okc) {
+                    ok = false;
+                    continue;
                 }
-                __syncthreads();
-                // scores: lane owns tokens lane and lane+32 of the tile
-                float z[2];
-#pragma unroll
-                for (int k = 0; k < 2; k++) {
-                    const int tok = lane + 32 * k;
-                    z[k] = NEG;
-                    if (tok < n) {
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-                        for (int i = 0; i < 16; i++) {
-                            const uint4 kk = *reinterpret_cast<const uint4 *>(Ks + tok * kBandRow + i * 16);
-                            const uint4 qq = qs[i];
-                            const uint32_t ka[4] = {kk.x, kk.y, kk.z, kk.w}, qa[4] = {qq.x, qq.y, qq.z, qq.w};
-#pragma unroll
-                            for (int jj = 0; jj < 4; jj++) {
-                                const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ka[jj]));
-                                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[jj]));
-                                acc[jj] = fmaf(kf.x, qf.x, acc[jj]);
-                                acc[jj] = fmaf(kf.y, qf.y, acc[jj]);
-                            }
-                        }
-                        z[k] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * L.scale_log2;
-                    }
-                }
-                const float tmax = warp_max(fmaxf(z[0], z[1]));
-                const float Mn = fmaxf(M, tmax);
-                const float al = exp2f(M - Mn);
-                const float p0 = exp2f(z[0] - Mn), p1 = exp2f(z[1] - Mn);
-                Ls = Ls * al + warp_sum(p0 + p1);
-                O = scale4(O, al);
-                for (int tok = 0; tok < n; tok++) {
-                    const float pt = __shfl_sync(0xffffffffu, tok < 32 ? p0 : p1, tok & 31);
-                    fma4(O, pt, load_bf16x4(reinterpret_cast<const __nv_bfloat16 *>(Vs + tok * kBandRow) + 4 * lane));
-                }
-                M = Mn;
+                const uint4 v = reinterpret_cast<const uint4 *>((isv ? L.v_pool : L.k_pool) + off)[ch];
+                *reinterpret_cast<uint4 *>((isv ? Vs : Ks) + tok * kBandRow + ch * 16) = v;
             }
-            lb = (M + log2f(Ls)) * kLn2;
-            ob = scale4(O, 1.f / Ls);
+            __syncthreads();
+            // scores: lane owns tokens lane and lane+32 of the tile
+            float z[2];
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const int tok = lane + 32 * k;
+                z[k] = NEG;
+                if (tok < n) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                    for (int i = 0; i < 16; i++) {
+                        const uint4 kk = *reinterpret_cast<const uint4 *>(Ks + tok * kBandRow + i * 16);
+                        const uint4 qq = qs[i];
+                        const uint32_t ka[4] = {kk.x, kk.y, kk.z, kk.w}, qa[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                        for (int jj = 0; jj < 4; jj++) {
+                            const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ka[jj]));
+                            const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[jj]));
+                            acc[jj] = fmaf(kf.x, qf.x, acc[jj]);
+                            acc[jj] = fmaf(kf.y, qf.y, acc[jj]);
+                        }
+                    }
+                    z[k] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * L.scale_log2;
+                }
+            }
+            const float tmax = warp_max(fmaxf(z[0], z[1]));
+            const float Mn = fmaxf(M, tmax);
+            const float al = exp2f(M - Mn);
+            const float p0 = exp2f(z[0] - Mn), p1 = exp2f(z[1] - Mn);
+            Ls = Ls * al + warp_sum(p0 + p1);
+            O = scale4(O, al);
+            for (int tok = 0; tok < n; tok++) {
+                const float pt = __shfl_sync(0xffffffffu, tok < 32 ? p0 : p1, tok & 31);
+                fma4(O, pt, load_bf16x4(reinterpret_cast<const __nv_bfloat16 *>(Vs + tok * kBandRow) + 4 * lane));
+            }
+            M = Mn;
         }
         if (!ok) {
             if (lane == 0) atomicOr(L.err, kErrPage);
         } else {
-            const float lf = L.as_full_lse[gw];
-            const float delta = fminf(lb - lf, 0.f);
-            const float cond = -expm1f(delta);   // 1 - e^delta
-            if (cond < kRemovalMinCond) {
-                oe = *reinterpret_cast<const float4 *>(L.as_pre_o + gw * kD + 4 * lane);
-                le = L.as_pre_lse[gw];
-                if (lane == 0) atomicAdd(&L.stats[kStDirect], 1ull);
-            } else {
-                const float wgt = expf(delta), inv_c = 1.f / cond;
-                const float4 of = *reinterpret_cast<const float4 *>(L.as_full_o + gw * kD + 4 * lane);
-                oe = make_float4((of.x - wgt * ob.x) * inv_c, (of.y - wgt * ob.y) * inv_c,
-                                 (of.z - wgt * ob.z) * inv_c, (of.w - wgt * ob.w) * inv_c);
-                le = lf + log1mexp_f(delta);
-            }
+            const float lb = (M + log2f(Ls)) * kLn2;
+            const float4 ob = scale4(O, 1.f / Ls);
+            const float4 of = *reinterpret_cast<const float4 *>(L.as_full_o + gw * kD + 4 * lane);
+            const float4 opre = *reinterpret_cast<const float4 *>(L.as_pre_o + gw * kD + 4 * lane);
+            if (remove_band(L.as_full_lse[gw], of, lb, ob, L.as_pre_lse[gw], opre, le, oe) && lane == 0)
+                atomicAdd(&L.stats[kStDirect], 1ull);
         }
     }
     const size_t e = gw * L.ring_len + slot;
@@ -1006,7 +1072,12 @@ cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm)
 
 cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    match_plan_kernel<<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
+    // up to 16 heads per group: a 512-thread bound leaves room for the ring
+    // entry held in registers during Match
+    if (L.G <= 16)
+        match_plan_kernel<512><<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
+    else
+        match_plan_kernel<1024><<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
     return cudaGetLastError();
 }
 
@@ -1035,8 +1106,7 @@ cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cu
 
 cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    const int warps = a.batch * L.H;
-    return launch_maybe_pdl(combine_kernel, dim3((warps + 3) / 4), dim3(128), 0, s, a.pdl != 0, L, a);
+    return launch_maybe_pdl(combine_kernel, dim3(a.batch * L.H), dim3(kCombineWarps * 32), 0, s, a.pdl != 0, L, a);
 }
 
 static size_t amend_smem(int G) { return (size_t)2 * kBandTile * kBandRow + (size_t)G * kD * 2; }
@@ -1049,8 +1119,7 @@ cudaError_t amend_kernel_config()
 
 cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    const size_t smem = L.amend_band ? amend_smem(L.G) : 0;
-    amend_kernel<<<dim3(L.Hkv, a.batch), L.G * 32, smem, s>>>(L, a);
+    amend_kernel<<<dim3(L.Hkv, a.batch), L.G * 32, amend_smem(L.G), s>>>(L, a);
     return cudaGetLastError();
 }
 
