@@ -511,24 +511,43 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
 //   O^T[128 x 8] += V^T[128 x 16] P^T[16 x 8]          8 x 2 mma (P split
 //   into bf16 hi + lo so P V keeps ~16 bits of P: the partials must be
 //   fp32-accurate because Amend's removal amplifies their error)
+//
+// Copy addressing: thread t of a lane group copies the 16-byte chunks
+// t + i * 32 NH of a page; its chunk column is fixed (t mod 16) and its rows
+// step by 2 NH, so every offset is a per-thread constant computed once.
 // ---------------------------------------------------------------------------
-template <int NW, int S>
+template <int NW, int S, int NH>
 __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int NP = NW / NH;
+    constexpr int GT = NH * 32;              // threads per page lane
+    constexpr int CPT = 256 / GT;            // 16-byte chunks of K (and of V) per thread per page
     const int G = L.G;
-    const int NH = (G + 7) >> 3;
-    const int NP = NW / NH;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ht = warp % NH, pl = warp / NH;
-    const int gthreads = NH * 32;
-    const int gtid = threadIdx.x - pl * gthreads;
+    const int gtid = threadIdx.x - pl * GT;
     uint8_t *lane_smem = smem + (size_t)pl * S * kStageBytes;
+    const uint32_t lane_smem_u32 = smem_u32(lane_smem);
     const int r4 = lane >> 2, c4 = lane & 3;
+    const float sl2 = L.scale_log2;
+
+    // per-thread copy offsets (bytes within a 4 KB page block / stage half)
+    const int cch = gtid & 15, crow0 = gtid >> 4;   // chunk column, first row
+    uint32_t dst_off[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; i++) {
+        const int row = crow0 + i * (GT / 16);
+        dst_off[i] = row * 256 + ((cch ^ (row & 7)) << 4);
+    }
+    const uint32_t src_off0 = crow0 * 256 + cch * 16;
+    // ldmatrix row bases
+    const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // K tile row (token) this lane addresses
+    const int vtok = (lane & 7) + 8 * (lane >> 4);         // V tile row (token) this lane addresses
+
     pdl_launch_dependents();
     pdl_wait();   // the work list comes from match_plan
     const int n_items = *L.n_items;
-    const float sl2 = L.scale_log2;
 
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int4 item = L.items[it];
@@ -571,20 +590,19 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 
         auto issue = [&](int k) {
             const int pg = pg0 + pl + k * NP;
-            uint8_t *st = lane_smem + (k % S) * kStageBytes;
+            const uint32_t st = lane_smem_u32 + (k % S) * kStageBytes;
             bool ok = true;
             const size_t off = kv_block(L, b, g, pg, ok);
             if (!ok) {
                 if (gtid == 0) atomicOr(L.err, kErrPage);
                 return;
             }
-            const char *ksrc = reinterpret_cast<const char *>(L.k_pool + off);
-            const char *vsrc = reinterpret_cast<const char *>(L.v_pool + off);
-            for (int c = gtid; c < 512; c += gthreads) {
-                const int isv = c >> 8, cc = c & 255, row = cc >> 4, ch = cc & 15;
-                const char *src = (isv ? vsrc : ksrc) + row * 256 + ch * 16;
-                cp_async16(smem_u32(st + isv * 4096 + row * 256 + ((ch ^ (row & 7)) << 4)), src);
-            }
+            const char *ksrc = reinterpret_cast<const char *>(L.k_pool + off) + src_off0;
+            const char *vsrc = reinterpret_cast<const char *>(L.v_pool + off) + src_off0;
+#pragma unroll
+            for (int i = 0; i < CPT; i++) cp_async16(st + dst_off[i], ksrc + i * (GT / 16) * 256);
+#pragma unroll
+            for (int i = 0; i < CPT; i++) cp_async16(st + 4096 + dst_off[i], vsrc + i * (GT / 16) * 256);
         };
 
 #pragma unroll
@@ -594,31 +612,30 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         }
         for (int k = 0; k < npl; k++) {
             cp_async_wait<S - 2>();
-            named_bar(1 + pl, gthreads);
+            named_bar(1 + pl, GT);
             if (k + S - 1 < npl) issue(k + S - 1);
             cp_async_commit();
 
-            const uint8_t *Ks = lane_smem + (k % S) * kStageBytes;
-            const uint8_t *Vs = Ks + 4096;
+            const uint32_t Ks = lane_smem_u32 + (k % S) * kStageBytes;
+            const uint32_t Vs = Ks + 4096;
             const int pg = pg0 + pl + k * NP;
 
             // S^T = K Q^T
             float s[4] = {0.f, 0.f, 0.f, 0.f};
             {
-                const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-                const uint32_t rbase = smem_u32(Ks + row * 256);
+                const uint32_t rbase = Ks + krow * 256;
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++) {
                     const int ch = 2 * kk + (lane >> 4);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(a0, a1, a2, a3, rbase + ((ch ^ (row & 7)) << 4));
+                    ldsm_x4(a0, a1, a2, a3, rbase + ((ch ^ (krow & 7)) << 4));
                     mma_bf16(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
                 }
             }
             // s[0]: token r4 head hc0; s[1]: token r4 head hc1; s[2], s[3]: token r4+8
             float z0 = s[0] * sl2, z1 = s[1] * sl2, z2 = s[2] * sl2, z3 = s[3] * sl2;
-            const int j0 = pg * 16 + r4, j1 = j0 + 8;
             if (pg * 16 < lo_max || pg * 16 + 16 > ihi) {
+                const int j0 = pg * 16 + r4, j1 = j0 + 8;
                 if (!(j0 >= lo0 && j0 < ihi)) z0 = -CUDART_INF_F;
                 if (!(j0 >= lo1 && j0 < ihi)) z1 = -CUDART_INF_F;
                 if (!(j1 >= lo0 && j1 < ihi)) z2 = -CUDART_INF_F;
@@ -633,20 +650,25 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
             const float bs0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
             const float bs1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-            const float al0 = exp2f(m0 - bs0), al1 = exp2f(m1 - bs1);
             const float p0 = exp2f(z0 - bs0), p1 = exp2f(z1 - bs1);
             const float p2 = exp2f(z2 - bs0), p3 = exp2f(z3 - bs1);
-            l0 = l0 * al0 + p0 + p2;
-            l1 = l1 * al1 + p1 + p3;
+            // rescale only when some running max moved (rare after the first pages)
+            if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+                const float al0 = exp2f(m0 - bs0), al1 = exp2f(m1 - bs1);
+                l0 *= al0;
+                l1 *= al1;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    acc[i][0] *= al0;
+                    acc[i][1] *= al1;
+                    acc[i][2] *= al0;
+                    acc[i][3] *= al1;
+                }
+            }
+            l0 += p0 + p2;
+            l1 += p1 + p3;
             m0 = mn0;
             m1 = mn1;
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al1;
-                acc[i][2] *= al0;
-                acc[i][3] *= al1;
-            }
             // P^T fragments (hi + lo bf16 parts) via in-register transpose
             const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
             const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
@@ -656,13 +678,12 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             const uint32_t bh0 = movmatrix_t(bf16x2_bits(h01)), bh1 = movmatrix_t(bf16x2_bits(h23));
             const uint32_t bl0 = movmatrix_t(bf16x2_bits(e01)), bl1 = movmatrix_t(bf16x2_bits(e23));
             {
-                const int tok = (lane & 7) + 8 * (lane >> 4);
-                const uint32_t vbase = smem_u32(Vs + tok * 256);
+                const uint32_t vbase = Vs + vtok * 256;
 #pragma unroll
                 for (int mt = 0; mt < 8; mt++) {
                     const int ch = 2 * mt + ((lane >> 3) & 1);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(a0, a1, a2, a3, vbase + ((ch ^ (tok & 7)) << 4));
+                    ldsm_x4_t(a0, a1, a2, a3, vbase + ((ch ^ (vtok & 7)) << 4));
                     mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
                     mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
                 }
@@ -702,9 +723,11 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         for (int idx = threadIdx.x; idx < G * kD; idx += NW * 32) {
             const int hh = idx / kD, dd = idx - hh * kD;
             float M = -CUDART_INF_F;
+#pragma unroll
             for (int q = 0; q < NP; q++) M = fmaxf(M, red_ml[q * G + hh].x);
             float lsum = 0.f, osum = 0.f;
             if (M != -CUDART_INF_F) {
+#pragma unroll
                 for (int q = 0; q < NP; q++) {
                     const float2 ml = red_ml[q * G + hh];
                     const float wq = exp2f(ml.x - M);
@@ -1053,21 +1076,33 @@ __global__ void append_kernel(Layout L, int req, int start, int n, const __nv_bf
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+static int head_tiles(int G) { return (G + 7) / 8; }
+
 static size_t attention_smem(int G)
 {
-    const int NH = (G + 7) / 8, NP = kAttnWarps / NH;
+    const int NH = head_tiles(G), NP = kAttnWarps / NH;
     const size_t pipe = (size_t)NP * kAttnStages * kStageBytes;
     const size_t red = (size_t)NP * G * kD * 4 + (size_t)NP * G * 8;
     return pipe > red ? pipe : red;
 }
 
+template <int NH>
+static cudaError_t attention_config_nh(size_t smem, int *ctas_per_sm)
+{
+    auto k = attention_kernel<kAttnWarps, kAttnStages, NH>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, k, kAttnWarps * 32, smem);
+}
+
 cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm)
 {
     *smem = attention_smem(G);
-    auto k = attention_kernel<kAttnWarps, kAttnStages>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*smem);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, k, kAttnWarps * 32, *smem);
+    switch (head_tiles(G)) {
+    case 1: return attention_config_nh<1>(*smem, ctas_per_sm);
+    case 2: return attention_config_nh<2>(*smem, ctas_per_sm);
+    default: return attention_config_nh<4>(*smem, ctas_per_sm);
+    }
 }
 
 cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s)
@@ -1100,8 +1135,12 @@ static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem
 
 cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)
 {
-    return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages>, dim3(a.grid_ctas), dim3(kAttnWarps * 32), smem,
-                            s, a.pdl != 0, L, a);
+    const dim3 grid(a.grid_ctas), block(kAttnWarps * 32);
+    switch (head_tiles(L.G)) {
+    case 1: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1>, grid, block, smem, s, a.pdl, L, a);
+    case 2: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2>, grid, block, smem, s, a.pdl, L, a);
+    default: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 4>, grid, block, smem, s, a.pdl, L, a);
+    }
 }
 
 cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
