@@ -15,8 +15,19 @@ constexpr int kMaxRing = 64;            // ring entries per (request, head)
 constexpr int kMaxGroup = 32;           // query heads per KV head
 constexpr int kMaxCtas = 1024;          // upper bound of the attention grid
 constexpr int kMaxGroupsPerStep = 8192; // max_batch * kv_heads
-constexpr int kAttnWarps = 4;           // warps per attention CTA
-constexpr int kAttnStages = 3;          // pipeline stages per page lane
+// attention pipeline shape (overridable at build time for tuning sweeps)
+#ifndef MAC_ATTN_WARPS
+#define MAC_ATTN_WARPS 4
+#endif
+#ifndef MAC_ATTN_STAGES
+#define MAC_ATTN_STAGES 3
+#endif
+#ifndef MAC_PREFETCH_AHEAD
+#define MAC_PREFETCH_AHEAD 4
+#endif
+constexpr int kAttnWarps = MAC_ATTN_WARPS;         // warps per attention CTA
+constexpr int kAttnStages = MAC_ATTN_STAGES;       // pipeline stages per page lane
+constexpr int kPrefetchAhead = MAC_PREFETCH_AHEAD; // pages per lane prefetched into L2 past the copy front
 constexpr int kStageBytes = 2 * kPage * kD * 2;   // one K page + one V page (bf16): 8 KB
 constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
 constexpr int kMinChunk = 64;           // smallest work-item span in tokens

@@ -82,6 +82,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -588,6 +594,17 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         const int npg = pg1 - pg0 + 1;
         const int npl = pl < npg ? (npg - pl + NP - 1) / NP : 0;
 
+        // L2 prefetch of the page kPrefetchAhead pages past the copy front:
+        // raises the bytes in flight beyond what the shared-memory stages hold
+        auto prefetch = [&](int k) {
+            if (gtid != 0 || k >= npl) return;
+            const int pg = pg0 + pl + k * NP;
+            bool ok = true;
+            const size_t off = kv_block(L, b, g, pg, ok);
+            if (!ok) return;
+            prefetch_l2_bulk(L.k_pool + off, 4096);
+            prefetch_l2_bulk(L.v_pool + off, 4096);
+        };
         auto issue = [&](int k) {
             const int pg = pg0 + pl + k * NP;
             const uint32_t st = lane_smem_u32 + (k % S) * kStageBytes;
@@ -606,6 +623,8 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         };
 
 #pragma unroll
+        for (int k = S - 1; k < S - 1 + kPrefetchAhead; k++) prefetch(k);
+#pragma unroll
         for (int k = 0; k < S - 1; k++) {
             if (k < npl) issue(k);
             cp_async_commit();
@@ -615,6 +634,7 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             named_bar(1 + pl, GT);
             if (k + S - 1 < npl) issue(k + S - 1);
             cp_async_commit();
+            prefetch(k + S - 1 + kPrefetchAhead);
 
             const uint32_t Ks = lane_smem_u32 + (k % S) * kStageBytes;
             const uint32_t Vs = Ks + 4096;
