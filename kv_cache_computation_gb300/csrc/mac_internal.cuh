@@ -23,7 +23,7 @@ constexpr int kMaxGroupsPerStep = 8192; // max_batch * kv_heads
 #define MAC_ATTN_STAGES 3
 #endif
 #ifndef MAC_PREFETCH_AHEAD
-#define MAC_PREFETCH_AHEAD 4
+#define MAC_PREFETCH_AHEAD 2
 #endif
 constexpr int kAttnWarps = MAC_ATTN_WARPS;         // warps per attention CTA
 constexpr int kAttnStages = MAC_ATTN_STAGES;       // pipeline stages per page lane
