@@ -204,6 +204,47 @@ mac_status mac_debug_get_decisions(mac_handle h, int batch, int32_t *host_slot, 
 mac_status mac_debug_read_ring(mac_handle h, int req, int32_t *host_pos, uint16_t *host_q, float *host_o,
                                float *host_lse, int64_t *kv_len, int64_t *steps);
 
+/* ---- decode attention without any device allocation --------------------- */
+
+/* No counterpart in the paper: this entry point exists for callers that may
+ * not allocate device memory at the point where they run attention -- a
+ * runtime that plans every byte of device memory in one arena at start-up
+ * and forbids later allocations, a latency-critical loop that must not call
+ * cudaMalloc (it can synchronise the device), or a plug-in host that hands
+ * the library nothing but its input and output buffers.  Every handle-based
+ * call above needs a scratch buffer allocated for mac_create; this one
+ * needs none.
+ *
+ * It computes what mac_full_step computes (full split-KV decode attention,
+ * out = AS_{1:len}(q) per request and query head) over a KV cache the caller
+ * holds, without appending to it:
+ *   dev_k, dev_v  bf16 [batch][kv_heads][ctx_stride][head_dim]; token j of
+ *                 request b, KV head g starts at element
+ *                 ((b * kv_heads + g) * ctx_stride + j) * head_dim
+ *                 (the contiguous layout of a mac_create handle with
+ *                 page_size 0, ctx_stride = max_ctx rounded up to 16)
+ *   host_lens     host int32 [batch], tokens of each request, 1..ctx_stride
+ *   dev_q         bf16 [batch][heads][head_dim], post-RoPE query
+ *   dev_out       bf16 [batch][heads][head_dim]; dev_lse fp32 [batch][heads]
+ *                 natural-log LSE, or NULL
+ *   sm_scale      score scale, 0 selects 1/sqrt(head_dim)
+ * Limits: head_dim 128, heads / kv_heads in {1, 2, 4, 8, 16, 32}, batch
+ * 1..64, ctx_stride a multiple of 16.  Its work list and partial summaries
+ * live in a fixed 16 MiB device array inside the library, which every GPU
+ * that loads the library holds until the process exits; a call whose
+ * scratch would exceed it returns MAC_ERR_CAPACITY and launches nothing.
+ * The first call on each device looks up that array's device address and
+ * the kernels' launch shapes (with that device current); make that first
+ * call before any stream capture.  All calls on a device share the array
+ * and overwrite it: calls whose GPU work can overlap (other streams, other
+ * host threads) race and must be serialised by the caller.  Async on
+ * stream; returns MAC_ERR_INVALID_ARG for bad arguments, MAC_ERR_CUDA if a
+ * launch fails. */
+mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, int head_dim, int64_t ctx_stride,
+                                 const void *dev_k, const void *dev_v, const int32_t *host_lens,
+                                 const void *dev_q, void *dev_out, float *dev_lse, float sm_scale,
+                                 void *stream);
+
 /* Human-readable text for a status code (static storage). */
 const char *mac_status_string(mac_status s);
 

@@ -60,6 +60,7 @@ SIGNATURES = {
     "mac_debug_force_decisions": (_i, [_vp, _vp, _i, _vp]),
     "mac_debug_get_decisions": (_i, [_vp, _i, _pi32, _pi32, _pf, _pf]),
     "mac_debug_read_ring": (_i, [_vp, _i, _pi32, _pu16, _pf, _pf, _pi64, _pi64]),
+    "mac_attention_noalloc": (_i, [_i, _i, _i, _i, _i64, _vp, _vp, _pi32, _vp, _vp, _vp, _f, _vp]),
     "mac_status_string": (ctypes.c_char_p, [_i]),
     "mac_last_error": (ctypes.c_char_p, [_vp]),
 }
