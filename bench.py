@@ -369,7 +369,8 @@ def bench_ours(args, ws, rank, local):
                      "traffic": traffic},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": int(4 * K_steps),
+        # per step: match_plan, attention, combine (+ the side-stream Amend when it recomputes the band)
+        "gpu_launches": int((3 + (1 if args.amend_band else 0)) * K_steps),
         "clocks": clk,
         "stats": {"removal_direct": st["removal_direct"], "device_error": st["device_error"],
                   "work_items_per_step": round(items / max(1, steps), 1)},
