@@ -69,7 +69,7 @@ typedef struct {
     int band_r;         /* r: rectification band width in tokens, >= 1           */
     double tau;         /* L2 threshold, relative: hit iff                       */
                         /* ||q~_m - q~_e|| < tau * ||q~_m||; tau >= 0           */
-    int max_batch;      /* request slots, >= 1                                   */
+    int max_batch;      /* request slots, >= 1; max_batch * kv_heads <= 1024    */
     int64_t max_ctx;    /* tokens per request, 1 .. 2^30                         */
     int page_size;      /* 0: contiguous KV per request; 16: paged KV            */
     int num_pages;      /* paged: pages in the pool (0: max_batch*ceil(max_ctx/16)) */
@@ -229,7 +229,7 @@ mac_status mac_debug_read_ring(mac_handle h, int req, int32_t *host_pos, uint16_
  *                 natural-log LSE, or NULL
  *   sm_scale      score scale, 0 selects 1/sqrt(head_dim)
  * Limits: head_dim 128, heads / kv_heads in {1, 2, 4, 8, 16, 32}, batch
- * 1..64, ctx_stride a multiple of 16.  Its work list and partial summaries
+ * 1..64, batch * kv_heads <= 1024, ctx_stride a multiple of 16.  Its work list and partial summaries
  * live in a fixed 16 MiB device array inside the library, which every GPU
  * that loads the library holds until the process exits; a call whose
  * scratch would exceed it returns MAC_ERR_CAPACITY and launches nothing.

@@ -46,7 +46,7 @@ struct Sizes {
     int G = 0, pages_per_req = 0, num_pages = 0, ctx_stride = 0, item_cap = 0;
     size_t r_pos, r_q, r_o, r_lse;
     size_t s_page, s_kvlen, s_step, s_mcur, s_slot, s_own_slot, s_own_hit, s_dslot, s_dlo, s_dD, s_dqn2,
-        s_forced, s_qstash, s_glo, s_goff, s_items, s_nitems, s_ticket, s_po, s_pml, s_afo, s_afl, s_apo,
+        s_forced, s_qstash, s_glo, s_goff, s_items, s_nitems, s_po, s_pml, s_afo, s_afl, s_apo,
         s_apl, s_stats, s_err;
 };
 
@@ -112,7 +112,6 @@ mac_status compute_sizes(const mac_config *c, Sizes *z)
     z->s_goff = s.take((BG + 1) * 4);
     z->s_items = s.take(cap * sizeof(int4));
     z->s_nitems = s.take(4);
-    z->s_ticket = s.take(4);
     z->s_po = s.take(cap * G * kD * 4);
     z->s_pml = s.take(cap * G * 8);
     z->s_afo = s.take(BH * kD * 4);
@@ -407,7 +406,6 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     L.grp_item_off = (int32_t *)(sc + z.s_goff);
     L.items = (int4 *)(sc + z.s_items);
     L.n_items = (int32_t *)(sc + z.s_nitems);
-    L.ticket = (uint32_t *)(sc + z.s_ticket);
     L.part_o = (float *)(sc + z.s_po);
     L.part_ml = (float2 *)(sc + z.s_pml);
     L.as_full_o = (float *)(sc + z.s_afo);

@@ -14,7 +14,7 @@ constexpr int kPage = 16;               // tokens per KV page / per staged block
 constexpr int kMaxRing = 64;            // ring entries per (request, head)
 constexpr int kMaxGroup = 32;           // query heads per KV head
 constexpr int kMaxCtas = 1024;          // upper bound of the attention grid
-constexpr int kMaxGroupsPerStep = 8192; // max_batch * kv_heads
+constexpr int kMaxGroupsPerStep = 1024; // max_batch * kv_heads (the plan is held in shared memory)
 // attention pipeline shape (overridable at build time for tuning sweeps)
 #ifndef MAC_ATTN_WARPS
 #define MAC_ATTN_WARPS 4
@@ -76,11 +76,10 @@ struct Layout {
     __nv_bfloat16 *q_stash;   // [max_batch][H][D] post-RoPE query kept for Amend
 
     // plan
-    int32_t *grp_lo;          // [max_batch * Hkv]
+    int32_t *grp_lo;          // [max_batch * Hkv] first token any head of the group reads
     int32_t *grp_item_off;    // [max_batch * Hkv + 1]
     int4 *items;              // [item_cap] {b*Hkv+g, lo, hi, segment}
     int32_t *n_items;
-    uint32_t *ticket;
 
     // partial summaries of work items: unnormalised o, (max, sum) in log2 units
     float *part_o;            // [item_cap][G][D]

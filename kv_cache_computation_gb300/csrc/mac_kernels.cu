@@ -208,12 +208,12 @@ __device__ __forceinline__ float warp_max(float v)
 }
 
 // ---------------------------------------------------------------------------
-// Planning (last block of match_plan).  Per (request, kv-head) group the
-// streamed span is [lo_g, m), lo_g being the smallest band+tail start of the
-// group's heads.  Amend's band [m-r, m) is cut off as its own segment, so
-// Complete yields the rectification term AS_{m-r+1:m} and the direct form of
-// AS_{1:m-r} as by-products.  Chunks are cut at multiples of C (a multiple of
-// 16: page aligned).
+// Planning (prologue of every attention CTA; all CTAs derive the same plan).
+// Per (request, kv-head) group the streamed span is [lo_g, m), lo_g being the
+// smallest band+tail start of the group's heads.  Amend's band [m-r, m) is
+// cut off as its own segment, so Complete yields the rectification term
+// AS_{m-r+1:m} and the direct form of AS_{1:m-r} as by-products.  Chunks are
+// cut at multiples of C (a multiple of 16: page aligned).
 //
 // Balanced mode (Figure 3(b), "load-balanced planning"): every item costs at
 // most C tokens, so the step finishes when the longest item does; the plan
@@ -222,43 +222,42 @@ __device__ __forceinline__ float warp_max(float v)
 // Longer spans thereby get proportionally more CTAs.  Equal mode gives every
 // group the same number of items whatever its span (unbalanced baseline).
 // ---------------------------------------------------------------------------
-__device__ void plan_work(const Layout &L, const StepArgs &a)
+struct PlanShared {
+    int lo[kPlanCache];
+    int hi[kPlanCache];
+    int off[kPlanCache + 1];
+    int C;
+    int total;
+    long long T, Tf;
+};
+
+__device__ __forceinline__ int plan_split(const Layout &L, const StepArgs &a, int lo, int hi)
 {
-    __shared__ int s_lo[kPlanCache], s_sp[kPlanCache], s_hi[kPlanCache];
-    __shared__ int s_C;
-    __shared__ long long s_T, s_Tf;
+    return a.full_mode ? lo : max(lo, hi - L.band_r);
+}
+
+__device__ __forceinline__ int plan_chunk(const Layout &L, const StepArgs &a, const PlanShared &ps, int nbg, int lo,
+                                          int hi)
+{
+    if (a.plan_mode == 0) return ps.C;
+    const int splits = a.grid_ctas / nbg > 1 ? a.grid_ctas / nbg : 1;
+    return max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
+}
+
+__device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
+{
     const int nbg = a.batch * L.Hkv;
-    const int nthr = blockDim.x;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const bool cached = nbg <= kPlanCache;
-    auto group = [&](int bg, int &lo, int &sp, int &hi) {
-        if (cached) {
-            lo = s_lo[bg];
-            sp = s_sp[bg];
-            hi = s_hi[bg];
-            return;
-        }
-        hi = __ldcg(&L.kv_len[bg / L.Hkv]) + 1;
-        lo = __ldcg(&L.grp_lo[bg]);
-        sp = a.full_mode ? lo : max(lo, hi - L.band_r);
-    };
-    if (cached) {
-        for (int bg = threadIdx.x; bg < nbg; bg += nthr) {
-            const int hi = __ldcg(&L.kv_len[bg / L.Hkv]) + 1;
-            const int lo = __ldcg(&L.grp_lo[bg]);
-            s_lo[bg] = lo;
-            s_hi[bg] = hi;
-            s_sp[bg] = a.full_mode ? lo : max(lo, hi - L.band_r);
-        }
+    for (int bg = threadIdx.x; bg < nbg; bg += blockDim.x) {
+        ps.hi[bg] = __ldcg(&L.m_cur[bg / L.Hkv]);   // m: the length after this step's append
+        ps.lo[bg] = __ldcg(&L.grp_lo[bg]);
     }
     __syncthreads();
-    const int splits = a.grid_ctas / nbg > 1 ? a.grid_ctas / nbg : 1;
     if (w == 0) {
         long long T = 0, Tf = 0;
         int nseg = 0;
         for (int bg = lane; bg < nbg; bg += 32) {
-            int lo, sp, hi;
-            group(bg, lo, sp, hi);
+            const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
             T += hi - lo;
             Tf += hi;
             nseg += (sp > lo) + (hi > sp);
@@ -273,8 +272,7 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
             auto count = [&](int Cc) {
                 int c = 0;
                 for (int bg = lane; bg < nbg; bg += 32) {
-                    int lo, sp, hi;
-                    group(bg, lo, sp, hi);
+                    const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
                     c += n_chunks(lo, sp, Cc) + n_chunks(sp, hi, Cc);
                 }
                 return warp_sum_int(c);
@@ -284,8 +282,7 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
             if (Q > L.item_cap) Q = L.item_cap;
             // count(C) < T/C + 2 nseg, so C >= T / (Q - 2 nseg) always fits Q items
             long long c_lo = round_up16((T + Q - 1) / Q);
-            long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg))
-                                            : (1ll << 30);
+            long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg)) : (1ll << 30);
             if (c_lo < kMinChunk) c_lo = kMinChunk;
             if (c_hi < c_lo) c_hi = c_lo;
             while (c_lo < c_hi) {
@@ -297,55 +294,58 @@ __device__ void plan_work(const Layout &L, const StepArgs &a)
             C = (int)c_hi;
         }
         if (lane == 0) {
-            s_C = C;
-            s_T = T;
-            s_Tf = Tf;
+            ps.C = C;
+            ps.T = T;
+            ps.Tf = Tf;
         }
     }
     __syncthreads();
-    const int sC = s_C;
-    // offsets and items; groups are taken in rounds so the list stays in order
+    // item offsets per group (block scan in rounds keeps the groups in order)
     int base = 0;
-    for (int r0 = 0; r0 < nbg; r0 += nthr) {
+    for (int r0 = 0; r0 < nbg; r0 += blockDim.x) {
         const int bg = r0 + threadIdx.x;
-        int cnt = 0, lo = 0, hi = 0, sp = 0, C = kMinChunk;
+        int cnt = 0;
         if (bg < nbg) {
-            group(bg, lo, sp, hi);
-            C = a.plan_mode == 0 ? sC : max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
+            const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
+            const int C = plan_chunk(L, a, ps, nbg, lo, hi);
             cnt = n_chunks(lo, sp, C) + n_chunks(sp, hi, C);
         }
         int tot;
         const int off = base + block_exclusive_scan(cnt, &tot);
-        if (bg < nbg) {
-            L.grp_item_off[bg] = off;
-            int k = off;
-            for (int seg = 0; seg < 2; seg++) {
-                const int s0 = seg == 0 ? lo : sp, s1 = seg == 0 ? sp : hi;
-                if (s1 <= s0) continue;
-                for (int c = s0 / C; c <= (s1 - 1) / C; c++)
-                    if (k < L.item_cap) L.items[k++] = make_int4(bg, max(s0, c * C), min(s1, (c + 1) * C), seg);
-            }
-        }
+        if (bg < nbg) ps.off[bg] = off;
         base += tot;
     }
     if (threadIdx.x == 0) {
-        if (base > L.item_cap) {   // cannot happen with the C chosen above; keep the list in bounds
-            atomicOr(L.err, kErrPos);
-            base = L.item_cap;
-        }
-        L.grp_item_off[nbg] = base;
-        *L.n_items = base;
-        atomicAdd(&L.stats[kStSteps], 1ull);
-        atomicAdd(&L.stats[kStKvRead], (unsigned long long)s_T);
-        atomicAdd(&L.stats[kStKvFull], (unsigned long long)s_Tf);
-        atomicAdd(&L.stats[kStItems], (unsigned long long)base);
-        if (!a.full_mode) atomicAdd(&L.stats[kStDecisions], (unsigned long long)a.batch * L.H);
-        *L.ticket = 0u;   // ready for the next launch
+        ps.off[nbg] = base;
+        ps.total = base < L.item_cap ? base : L.item_cap;
     }
+    __syncthreads();
+}
+
+// Work item `it` of the plan: {group, lo, hi, segment}.
+__device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &ps, int nbg, int it)
+{
+    int g0 = 0, g1 = nbg - 1;   // the last group whose first item is <= it
+    while (g0 < g1) {
+        const int mid = (g0 + g1 + 1) >> 1;
+        if (ps.off[mid] <= it) g0 = mid;
+        else g1 = mid - 1;
+    }
+    const int bg = g0, k = it - ps.off[bg];
+    const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
+    const int C = plan_chunk(L, a, ps, nbg, lo, hi);
+    const int nA = n_chunks(lo, sp, C);
+    if (k < nA) {
+        const int c = lo / C + k;
+        return make_int4(bg, max(lo, c * C), min(sp, (c + 1) * C), 0);
+    }
+    const int c = sp / C + (k - nA);
+    return make_int4(bg, max(sp, c * C), min(hi, (c + 1) * C), 1);
 }
 
 // ---------------------------------------------------------------------------
 // match_plan: grid (Hkv, batch), block G warps (warp w = query head g*G + w).
+// Leaves per group the span start lo_g; the attention kernel plans from it.
 // Match (Figure 2(a)): lane e evaluates ring entry e (and e+32), so all the
 // ring's loads are in flight at once; a warp argmin then picks the nearest
 // entry (ties to the larger position).
@@ -486,23 +486,15 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
         L.slot_cur[b] = slot_new;
     }
 
-    // group span start = min over the group's heads; then the ticket
+    // group span start = min over the group's heads
     __shared__ int s_glo[32];
-    __shared__ int s_last;
     if (lane == 0) s_glo[w] = lo_h;
     __syncthreads();
     if (threadIdx.x == 0) {
         int lo = s_glo[0];
         for (int i = 1; i < G; i++) lo = min(lo, s_glo[i]);
         L.grp_lo[(size_t)b * L.Hkv + g] = lo;
-        __threadfence();
-        const unsigned t = atomicAdd(L.ticket, 1u);
-        s_last = (t == gridDim.x * gridDim.y - 1);
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    plan_work(L, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -551,12 +543,28 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // K tile row (token) this lane addresses
     const int vtok = (lane & 7) + 8 * (lane >> 4);         // V tile row (token) this lane addresses
 
+    __shared__ PlanShared ps;
     pdl_launch_dependents();
-    pdl_wait();   // the work list comes from match_plan
-    const int n_items = *L.n_items;
+    pdl_wait();   // spans come from match_plan
+    cta_plan(L, a, ps);
+    const int nbg = a.batch * L.Hkv;
+    const int n_items = ps.total;
+    if (blockIdx.x == 0) {   // publish the plan for combine and the counters
+        for (int i = threadIdx.x; i <= nbg; i += blockDim.x) L.grp_item_off[i] = min(ps.off[i], n_items);
+        for (int i = threadIdx.x; i < n_items; i += blockDim.x) L.items[i] = plan_item(L, a, ps, nbg, i);
+        if (threadIdx.x == 0) {
+            *L.n_items = n_items;
+            if (ps.off[nbg] > L.item_cap) atomicOr(L.err, kErrPos);
+            atomicAdd(&L.stats[kStSteps], 1ull);
+            atomicAdd(&L.stats[kStKvRead], (unsigned long long)ps.T);
+            atomicAdd(&L.stats[kStKvFull], (unsigned long long)ps.Tf);
+            atomicAdd(&L.stats[kStItems], (unsigned long long)n_items);
+            if (!a.full_mode) atomicAdd(&L.stats[kStDecisions], (unsigned long long)a.batch * L.H);
+        }
+    }
 
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int4 item = L.items[it];
+        const int4 item = plan_item(L, a, ps, nbg, it);
         const int bg = item.x, ilo = item.y, ihi = item.z;
         const int b = bg / L.Hkv, g = bg - b * L.Hkv;
 

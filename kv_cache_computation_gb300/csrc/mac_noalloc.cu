@@ -56,7 +56,7 @@ int group_index(int G)
 }
 
 struct NoallocPlanArgs {
-    int batch, kv_heads, grid_ctas, item_cap;
+    int batch, kv_heads;
     int lens[kNoallocMaxBatch];
 };
 
@@ -64,7 +64,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Byte offsets of the scratch regions for one call.
 struct NoallocCarve {
-    size_t items, n_items, goff, dec_lo, m_cur, kv_len, stats, err, part_ml, part_o, total;
+    size_t items, n_items, goff, glo, dec_lo, m_cur, kv_len, stats, err, part_ml, part_o, total;
 };
 
 NoallocCarve carve(int batch, int heads, int kv_heads, int item_cap)
@@ -80,6 +80,7 @@ NoallocCarve carve(int batch, int heads, int kv_heads, int item_cap)
     c.items = take((size_t)item_cap * sizeof(int4));
     c.n_items = take(4);
     c.goff = take(((size_t)batch * kv_heads + 1) * 4);
+    c.glo = take((size_t)batch * kv_heads * 4);
     c.dec_lo = take((size_t)batch * heads * 4);
     c.m_cur = take((size_t)batch * 4);
     c.kv_len = take((size_t)batch * 4);
@@ -91,42 +92,12 @@ NoallocCarve carve(int batch, int heads, int kv_heads, int item_cap)
     return c;
 }
 
-// One block: a work list cutting every request's [0, len) into page-aligned
-// chunks of C tokens, C chosen so the list fits the attention grid.
-__global__ void noalloc_plan_kernel(Layout L, NoallocPlanArgs p)
+// One block: the span of every (request, KV head) group is [0, len); the
+// attention kernel plans its work items from these.
+__global__ void noalloc_prepare_kernel(Layout L, NoallocPlanArgs p)
 {
-    __shared__ int s_C;
     const int nbg = p.batch * p.kv_heads;
-    if (threadIdx.x == 0) {
-        long long T = 0;
-        for (int b = 0; b < p.batch; b++) T += (long long)p.lens[b] * p.kv_heads;
-        // ceil(len / C) <= len / C + 1 per group
-        const long long slots = p.grid_ctas > nbg ? p.grid_ctas - nbg : p.grid_ctas;
-        long long C = (T + slots - 1) / slots;
-        C = (C + 15) / 16 * 16;
-        if (C < kMinChunk) C = kMinChunk;
-        for (;;) {   // guard the capacity (never loops with the choice above)
-            long long n = 0;
-            for (int b = 0; b < p.batch; b++) n += (long long)p.kv_heads * ((p.lens[b] + C - 1) / C);
-            if (n <= p.item_cap) break;
-            C *= 2;
-        }
-        s_C = (int)C;
-        int off = 0;
-        for (int bg = 0; bg < nbg; bg++) {
-            L.grp_item_off[bg] = off;
-            off += (p.lens[bg / p.kv_heads] + s_C - 1) / s_C;
-        }
-        L.grp_item_off[nbg] = off;
-        *L.n_items = off;
-    }
-    __syncthreads();
-    const int C = s_C;
-    for (int bg = threadIdx.x; bg < nbg; bg += blockDim.x) {
-        const int b = bg / p.kv_heads, len = p.lens[b];
-        int k = L.grp_item_off[bg];
-        for (int c0 = 0; c0 < len; c0 += C) L.items[k++] = make_int4(bg, c0, min(len, c0 + C), 1);
-    }
+    for (int bg = threadIdx.x; bg < nbg; bg += blockDim.x) L.grp_lo[bg] = 0;
     for (int i = threadIdx.x; i < p.batch * L.H; i += blockDim.x) L.dec_lo[i] = 0;
     for (int b = threadIdx.x; b < p.batch; b += blockDim.x) L.m_cur[b] = p.lens[b];
 }
@@ -168,7 +139,7 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
 {
     if (batch < 1 || batch > kNoallocMaxBatch || heads < 1 || kv_heads < 1 || heads % kv_heads) return MAC_ERR_INVALID_ARG;
     const int G = heads / kv_heads, gi = group_index(G);
-    if (gi < 0 || head_dim != kD) return MAC_ERR_INVALID_ARG;
+    if (gi < 0 || head_dim != kD || batch * kv_heads > kMaxGroupsPerStep) return MAC_ERR_INVALID_ARG;
     if (ctx_stride < kPage || ctx_stride % kPage || ctx_stride > (int64_t(1) << 30)) return MAC_ERR_INVALID_ARG;
     if (!dev_k || !dev_v || !host_lens || !dev_q || !dev_out) return MAC_ERR_INVALID_ARG;
     if ((((uintptr_t)dev_k | (uintptr_t)dev_v | (uintptr_t)dev_q | (uintptr_t)dev_out) & 15) || ((uintptr_t)dev_lse & 3))
@@ -191,8 +162,6 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
     const int item_cap = grid + 2 * batch * kv_heads;
     const NoallocCarve c = carve(batch, heads, kv_heads, item_cap);
     if (c.total > kNoallocScratchBytes) return MAC_ERR_CAPACITY;   // beyond the fixed scratch: nothing launched
-    pa.grid_ctas = grid;
-    pa.item_cap = item_cap;
 
     unsigned char *sc = s->scratch;
     Layout L{};
@@ -212,6 +181,7 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
     L.items = (int4 *)(sc + c.items);
     L.n_items = (int32_t *)(sc + c.n_items);
     L.grp_item_off = (int32_t *)(sc + c.goff);
+    L.grp_lo = (int32_t *)(sc + c.glo);
     L.dec_lo = (int32_t *)(sc + c.dec_lo);
     L.m_cur = (int32_t *)(sc + c.m_cur);
     L.kv_len = (int32_t *)(sc + c.kv_len);
@@ -233,7 +203,7 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
     cudaStream_t cs = (cudaStream_t)stream;
     // counters and the error word only accumulate: start them at zero
     if (cudaMemsetAsync(sc + c.stats, 0, c.err + 4 - c.stats, cs) != cudaSuccess) return MAC_ERR_CUDA;
-    noalloc_plan_kernel<<<1, 256, 0, cs>>>(L, pa);
+    noalloc_prepare_kernel<<<1, 256, 0, cs>>>(L, pa);
     if (cudaGetLastError() != cudaSuccess) return MAC_ERR_CUDA;
     if (launch_attention(L, a, s->smem[gi], cs) != cudaSuccess) return MAC_ERR_CUDA;
     if (launch_combine(L, a, cs) != cudaSuccess) return MAC_ERR_CUDA;

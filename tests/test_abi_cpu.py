@@ -79,7 +79,7 @@ def test_ring_layout_reproduces_table7():
                                  dict(tau=float("inf")), dict(max_batch=0), dict(max_ctx=0),
                                  dict(max_ctx=(1 << 30) + 1), dict(page_size=8), dict(plan_mode=2),
                                  dict(heads=64, kv_heads=1), dict(sm_scale=-1.0),
-                                 dict(amend_band=2)])
+                                 dict(amend_band=2), dict(max_batch=129, kv_heads=8)])
 def test_invalid_configs_are_rejected(native, bad):
     st, *_ = _sizes(native, _cfg(native, **bad))
     assert st == -1
