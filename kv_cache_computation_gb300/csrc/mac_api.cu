@@ -260,9 +260,16 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
     // predecessor's tail; event records between the kernels (profiling)
     // would sit between them, so it is used only when not profiling.
     a.pdl = pe ? 0 : 1;
+    // Match follows the previous step's combine directly in the stream only
+    // when no side-stream Amend wait sits between them
+    const bool waited = h->amend_pending;
 
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[0], s));
-    MAC_CUDA(h, launch_match_plan(h->lay, a, s));
+    {
+        StepArgs am = a;
+        am.pdl = (a.pdl && !waited) ? 1 : 0;
+        MAC_CUDA(h, launch_match_plan(h->lay, am, s));
+    }
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[1], s));
     MAC_CUDA(h, launch_attention(h->lay, a, h->attn_smem, s));
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[2], s));

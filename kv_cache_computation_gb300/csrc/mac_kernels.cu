@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
 {
     __shared__ __align__(16) uint4 s_q[32][16];
     pdl_launch_dependents();
+    pdl_wait();   // launched early behind the previous step: read nothing before its completion
     const int g = blockIdx.x, b = blockIdx.y;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = L.G, H = L.H;
@@ -829,6 +830,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
     const int g = h / L.G, hh = h - g * L.G;
     const int bg = b * L.Hkv + g;
     const float NEG = -CUDART_INF_F;
+    pdl_launch_dependents();
     pdl_wait();   // partials come from the attention kernel
 
     float m_ring = NEG;
@@ -845,35 +847,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
         }
     }
     const int off0 = L.grp_item_off[bg], off1 = L.grp_item_off[bg + 1];
-    // block-wide maxima per segment
-    float mp = m_ring, mb = NEG;
-    for (int i = off0 + threadIdx.x; i < off1; i += blockDim.x) {
-        const float mi = L.part_ml[(size_t)i * L.G + hh].x;
-        if (L.items[i].w) mb = fmaxf(mb, mi);
-        else mp = fmaxf(mp, mi);
-    }
-    mp = warp_max(mp);
-    mb = warp_max(mb);
-    if (lane == 0) {
-        s_red[0][w] = mp;
-        s_red[1][w] = mb;
-    }
-    __syncthreads();
-    mp = s_red[0][0];
-    mb = s_red[1][0];
-#pragma unroll
-    for (int i = 1; i < kCombineWarps; i++) {
-        mp = fmaxf(mp, s_red[0][i]);
-        mb = fmaxf(mb, s_red[1][i]);
-    }
-    const float bp = mp == NEG ? 0.f : mp, bb = mb == NEG ? 0.f : mb;
-    // each warp's weighted sums over items w, w + kCombineWarps, ...
-    float lp = 0.f, lb = 0.f;
+    // One pass: each warp merges items w, w + kCombineWarps, ... (segment 0
+    // and segment 1 separately) online, rescaling its sums when a batch
+    // raises a maximum; a shared-memory step then merges the warps.
+    float mp = NEG, mb = NEG, lp = 0.f, lb = 0.f;
     float4 op = make_float4(0.f, 0.f, 0.f, 0.f), ob = op;
-    if (w == 0 && m_ring != NEG) {
-        const float wr = exp2f(m_ring - bp);
-        lp = wr;
-        op = scale4(o_ring, wr);
+    if (w == 0 && m_ring != NEG) {   // the reused AS_{1:p-r}: weight 1 at its own maximum
+        mp = m_ring;
+        lp = 1.f;
+        op = o_ring;
     }
     constexpr int kBatch = 4;
     for (int i0 = off0 + w; i0 < off1; i0 += kBatch * kCombineWarps) {
@@ -886,22 +868,43 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
             ml[k] = L.part_ml[(size_t)i * L.G + hh];
             sg[k] = L.items[i].w;
             ov[k] = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
+            if (i0 + k * kCombineWarps >= off1) ml[k].x = NEG;   // padding slot
+        }
+        float np = mp, nb = mb;
+#pragma unroll
+        for (int k = 0; k < kBatch; k++) {
+            if (sg[k]) nb = fmaxf(nb, ml[k].x);
+            else np = fmaxf(np, ml[k].x);
+        }
+        if (np != mp) {
+            const float r = mp == NEG ? 0.f : exp2f(mp - np);
+            lp *= r;
+            op = scale4(op, r);
+            mp = np;
+        }
+        if (nb != mb) {
+            const float r = mb == NEG ? 0.f : exp2f(mb - nb);
+            lb *= r;
+            ob = scale4(ob, r);
+            mb = nb;
         }
 #pragma unroll
         for (int k = 0; k < kBatch; k++) {
-            if (i0 + k * kCombineWarps >= off1) break;
-            const float wi = exp2f(ml[k].x - (sg[k] ? bb : bp));
+            if (ml[k].x == NEG) continue;
             if (sg[k]) {
+                const float wi = exp2f(ml[k].x - mb);
                 lb = fmaf(ml[k].y, wi, lb);
                 fma4(ob, wi, ov[k]);
             } else {
+                const float wi = exp2f(ml[k].x - mp);
                 lp = fmaf(ml[k].y, wi, lp);
                 fma4(op, wi, ov[k]);
             }
         }
     }
-    __syncthreads();   // s_red reused
     if (lane == 0) {
+        s_red[0][w] = mp;
+        s_red[1][w] = mb;
         s_l[0][w] = lp;
         s_l[1][w] = lb;
     }
@@ -909,18 +912,29 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
     s_o[1][w][lane] = ob;
     __syncthreads();
     if (w != 0) return;
-    lp = s_l[0][0];
-    lb = s_l[1][0];
-    op = s_o[0][0][lane];
-    ob = s_o[1][0][lane];
+    float bp = NEG, bb = NEG;
 #pragma unroll
-    for (int i = 1; i < kCombineWarps; i++) {
-        lp += s_l[0][i];
-        lb += s_l[1][i];
-        const float4 x = s_o[0][i][lane], y = s_o[1][i][lane];
-        op.x += x.x; op.y += x.y; op.z += x.z; op.w += x.w;
-        ob.x += y.x; ob.y += y.y; ob.z += y.z; ob.w += y.w;
+    for (int i = 0; i < kCombineWarps; i++) {
+        bp = fmaxf(bp, s_red[0][i]);
+        bb = fmaxf(bb, s_red[1][i]);
     }
+    lp = lb = 0.f;
+    op = ob = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kCombineWarps; i++) {
+        if (s_red[0][i] != NEG) {
+            const float r = exp2f(s_red[0][i] - bp);
+            lp = fmaf(s_l[0][i], r, lp);
+            fma4(op, r, s_o[0][i][lane]);
+        }
+        if (s_red[1][i] != NEG) {
+            const float r = exp2f(s_red[1][i] - bb);
+            lb = fmaf(s_l[1][i], r, lb);
+            fma4(ob, r, s_o[1][i][lane]);
+        }
+    }
+    if (bp == NEG) bp = 0.f;
+    if (bb == NEG) bb = 0.f;
     // AS_{1:m} = pre (+) band
     const float mf = fmaxf(lp > 0.f ? bp : NEG, lb > 0.f ? bb : NEG);
     const float wp = lp > 0.f ? exp2f(bp - mf) : 0.f, wb = lb > 0.f ? exp2f(bb - mf) : 0.f;
@@ -1133,16 +1147,7 @@ cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm)
     }
 }
 
-cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s)
-{
-    // up to 16 heads per group: a 512-thread bound leaves room for the ring
-    // entry held in registers during Match
-    if (L.G <= 16)
-        match_plan_kernel<512><<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
-    else
-        match_plan_kernel<1024><<<dim3(L.Hkv, a.batch), L.G * 32, 0, s>>>(L, a);
-    return cudaGetLastError();
-}
+
 
 template <typename Kernel>
 static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
@@ -1159,6 +1164,15 @@ static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, k, L, a);
+}
+
+cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s)
+{
+    // up to 16 heads per group: a 512-thread bound leaves room for the ring
+    // entry held in registers during Match
+    const dim3 grid(L.Hkv, a.batch), block(L.G * 32);
+    if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512>, grid, block, 0, s, a.pdl, L, a);
+    return launch_maybe_pdl(match_plan_kernel<1024>, grid, block, 0, s, a.pdl, L, a);
 }
 
 cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)
