@@ -1,7 +1,11 @@
 """Benchmark of the MAC-Attention decode step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--band-r R]
+                    [--workload NAME] [--band-r R] [--amend-band 0|1]
+
+Workloads: gqa_128k_b1_hetero (default), gqa_32k_b8_paged, gqa_4k_b1_contig,
+qwen_stack_120k_b4 (48-layer stack, --tau 0.3|0.45), sweep (forced hit rate x
+context x batch, MQA and GQA; one JSON line per point).
 
 A step is one MAC decode step (KV append, Match, planning, split-KV
 Complete, merge, Amend) for every request of the workload, on inputs already
@@ -384,6 +388,196 @@ def bench_ours(args, ws, rank, local):
     return result
 
 
+def _kv_bytes(stats):
+    return stats["kv_tokens_read"] * BYTES_PER_KV_TOKEN, stats["kv_tokens_full"] * BYTES_PER_KV_TOKEN
+
+
+def bench_stack(args, ws, rank, local):
+    """Qwen3-30B-A3B-shaped attention stack: one handle per layer, a step is
+    one decode step of every layer (Amend of layer l overlaps layers l+1..
+    when it runs on the side stream)."""
+    from kv_cache_computation_gb300 import MacAttention
+    from kv_cache_computation_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K_steps, W_steps = args.steps, args.warmup
+    prof_steps = min(K_steps, 16)
+    total = W_steps + K_steps + prof_steps + 1
+    cfg = W.qwen_moe_stack_120k_b4(steps=total, tau=args.tau if args.tau is not None else 0.3, layers=args.layers)
+    B, H, Hkv, G = cfg.batch, cfg.heads, cfg.kv_heads, cfg.group
+    max_ctx = cfg.context + total
+    ppr = (max_ctx + 15) // 16
+    pt = W.page_tables(B, ppr, seed=cfg.seed).to(dev)
+    macs, inps = [], []
+    for layer in range(cfg.layers):
+        mac = MacAttention(H, Hkv, cfg.head_dim, cfg.ring_len, cfg.band_r, cfg.tau, max_batch=B, max_ctx=max_ctx,
+                           page_size=16, plan_mode=args.plan_mode, amend_band=args.amend_band)
+        for b in range(B):
+            mac.set_page_table(b, pt[b].contiguous())
+        Kp, Vp = W.prefill_kv(cfg, layer=layer, device=dev)
+        for b in range(B):
+            mac.append_kv(b, Kp[b].contiguous(), Vp[b].contiguous())
+        del Kp, Vp
+        macs.append(mac)
+        inps.append(W.decode_inputs(cfg, layer=layer, device=dev))
+    out = torch.empty((B, H, cfg.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+
+    def run(t0, n):
+        for t in range(t0, t0 + n):
+            for mac, inp in zip(macs, inps):
+                mac.decode_step(inp["q_pre"][t], inp["q_post"][t], inp["k_new"][t], inp["v_new"][t], out=out, lse=lse)
+
+    run(0, W_steps)
+    for m in macs:
+        m.sync()
+    torch.cuda.synchronize()
+    for m in macs:
+        m.reset_stats()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        run(W_steps, K_steps)
+        for m in macs:
+            m.join()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    clk = clocks.summary()
+    sts = [m.stats() for m in macs]
+    kv_read = sum(_kv_bytes(st)[0] for st in sts)
+    kv_full = sum(_kv_bytes(st)[1] for st in sts)
+    hits = sum(st["hits"] for st in sts)
+    dec = sum(st["head_decisions"] for st in sts)
+    # per-kernel durations on a second pass with events around every launch
+    for m in macs:
+        m.reset_stats()
+        m.set_profiling(True)
+    run(W_steps + K_steps, prof_steps)
+    for m in macs:
+        m.join()
+    torch.cuda.synchronize()
+    profs = [m.profile() for m in macs]
+    sts_p = [m.stats() for m in macs]
+    for m in macs:
+        m.set_profiling(False)
+    attn_ms = sum(p_["attention_ms"] for p_ in profs)
+    launches = sum(p_["steps"] for p_ in profs)
+    attn_bytes = sum(st["kv_tokens_read"] * BYTES_PER_KV_TOKEN + st["steps"] * B * H * 256
+                     + st["work_items"] * G * (128 * 4 + 8) for st in sts_p)
+    peak, peak_kind = measured_peaks()
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    us = ms * 1e3 / K_steps
+    res = {
+        "metric": METRIC, "value": round(us, 2), "unit": "us/step", "n_gpus": ws, "steps": K_steps,
+        "warmup": W_steps, "ms_per_step": round(us / 1e3, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "batch": B, "context": cfg.context, "heads": H,
+                   "kv_heads": Hkv, "head_dim": cfg.head_dim, "ring_len": cfg.ring_len, "band_r": cfg.band_r,
+                   "tau": cfg.tau, "page_size": 16, "amend_band": args.amend_band,
+                   "l2": "inputs larger than L2", "step": "one decode step of every layer"},
+        "tokens_per_s": round(sum_over_ranks(B, ws, dev) / (us * 1e-6), 1),
+        "hbm_gbs_step": round(kv_read / K_steps / (us * 1e-6) / 1e9, 1),
+        "kv_bytes_read_vs_full": round(kv_read / kv_full, 5),
+        "hit_rate": round(hits / max(1, dec), 5),
+        "phase_us_per_layer_step": {k.replace("_ms", ""): round(sum(p_[k] for p_ in profs) * 1e3 / launches, 3)
+                                    for k in ("match_plan_ms", "attention_ms", "combine_ms", "amend_ms")},
+        "roofline": {"kernel": "attention_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "avg_launch_us": round(attn_ms * 1e3 / launches, 3), "traffic": None},
+        "gpu_launches": int((3 + (1 if args.amend_band else 0)) * K_steps * cfg.layers),
+        "clocks": clk,
+    }
+    for m in macs:
+        m.close()
+    return res
+
+
+def bench_sweep(args, ws, rank, local):
+    """Context x batch x forced hit rate, MQA and GQA: the MAC path against the
+    build's own full split-KV decode (mac_full_step) on the same handle.
+    Prints one JSON line per point (rank 0)."""
+    from kv_cache_computation_gb300 import MacAttention
+    from kv_cache_computation_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    steps, warm = args.steps, args.warmup
+    stream = torch.cuda.current_stream()
+    ctxs = [int(x) for x in args.sweep_contexts.split(",")]
+    batches = [int(x) for x in args.sweep_batches.split(",")]
+    rates = [float(x) for x in args.sweep_rates.split(",")]
+    kvs = [int(x) for x in args.sweep_kv_heads.split(",")]
+
+    def timed(fn, t0, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for t in range(t0, t0 + n):
+            fn(t)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    for kv in kvs:
+        for ctx in ctxs:
+            for B in batches:
+                base = W.sweep_point(ctx, B, 0.0, kv, steps=steps + 1)
+                H = base.heads
+                max_ctx = ctx + steps + 2
+                mac = MacAttention(H, kv, 128, base.ring_len, base.band_r, base.tau, max_batch=B, max_ctx=max_ctx,
+                                   page_size=16)
+                pt = W.page_tables(B, (max_ctx + 15) // 16, seed=base.seed).to(dev)
+                for b in range(B):
+                    mac.set_page_table(b, pt[b].contiguous())
+                Kp, Vp = W.prefill_kv(base, device=dev)
+                out = torch.empty((B, H, 128), dtype=torch.bfloat16, device=dev)
+                lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+
+                def restart():
+                    mac.sync()
+                    for b in range(B):
+                        mac.reset_request(b)
+                        mac.append_kv(b, Kp[b], Vp[b])
+                    torch.cuda.synchronize()
+
+                restart()
+                inp0 = W.decode_inputs(base, device=dev)
+                full_us = timed(lambda t: mac.full_step(inp0["q_post"][t], inp0["k_new"][t], inp0["v_new"][t],
+                                                        out=out, lse=lse), 0, steps)
+                for rate in rates:
+                    cfg = W.sweep_point(ctx, B, rate, kv, steps=steps + 1)
+                    inp = W.decode_inputs(cfg, device=dev)
+                    restart()
+                    step = lambda t: mac.decode_step(inp["q_pre"][t], inp["q_post"][t], inp["k_new"][t],
+                                                     inp["v_new"][t], out=out, lse=lse)
+                    for t in range(warm):
+                        step(t)
+                    mac.sync()
+                    mac.reset_stats()
+                    mac_us = timed(step, warm, steps - warm)
+                    mac.join()
+                    st = mac.stats()
+                    kv_read, kv_full = _kv_bytes(st)
+                    line = {"workload": "forced_hit_sweep", "kind": "mqa" if kv == 1 else "gqa", "heads": H,
+                            "kv_heads": kv, "context": ctx, "batch": B, "forced_hit": rate,
+                            "mac_us_step": round(mac_us, 2), "full_us_step": round(full_us, 2),
+                            "speedup_vs_full": round(full_us / mac_us, 3),
+                            "kv_bytes_read_vs_full": round(kv_read / max(1, kv_full), 4),
+                            "head_hit_rate": round(st["hits"] / max(1, st["head_decisions"]), 4),
+                            "mac_kv_gbs": round(kv_read / (steps - warm) / (mac_us * 1e-6) / 1e9, 1),
+                            "full_kv_gbs": round(kv_full / (steps - warm) / (full_us * 1e-6) / 1e9, 1)}
+                    if rank == 0:
+                        print(json.dumps(line), flush=True)
+                del Kp, Vp
+                mac.close()
+                torch.cuda.empty_cache()
+    return None
+
+
 def bench_reference(args, ws, rank, local):
     """The fp64 oracle on the host cores (rank 0 only)."""
     if rank != 0:
@@ -421,12 +615,22 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tau", type=float, default=None, help="threshold for the layer-stack workload (0.3 or 0.45)")
+    ap.add_argument("--layers", type=int, default=48, help="layers of the stack workload")
+    ap.add_argument("--sweep-contexts", default="4096,16384,65536,131072")
+    ap.add_argument("--sweep-batches", default="1,8,32")
+    ap.add_argument("--sweep-rates", default="0,0.5,0.9,1.0")
+    ap.add_argument("--sweep-kv-heads", default="1,8")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     ws, rank, local = dist_init()
     if args.impl == "reference":
         res = bench_reference(args, ws, rank, local)
+    elif args.workload == "qwen_stack_120k_b4":
+        res = bench_stack(args, ws, rank, local)
+    elif args.workload == "sweep":
+        res = bench_sweep(args, ws, rank, local)
     else:
         res = bench_ours(args, ws, rank, local)
     if rank == 0 and res is not None:
