@@ -239,7 +239,7 @@ def bench_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K_steps, W_steps = args.steps, args.warmup
-    total_steps = W_steps + 3 * K_steps + 2
+    total_steps = W_steps + 4 * K_steps + 2
     cfg = workload(args.workload, args.band_r, total_steps)
     B, H, Hkv, G = cfg.batch, cfg.heads, cfg.kv_heads, cfg.group
 
@@ -268,15 +268,32 @@ def bench_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     mac.reset_stats()
 
-    # timed region: K steps, device events on the launching stream
+    # Timed region: the K-step decode loop, captured once into a CUDA graph
+    # (as a serving loop runs it; capture itself is untimed) and replayed;
+    # device events on the launching stream.  --eager times per-call launches.
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for t in range(W_steps, W_steps + K_steps):
+                    mac.decode_step(*step_args(t), out=out, lse=lse)
+                mac.join()
+        torch.cuda.synchronize()
+        mac.reset_stats()
     with ClockSampler(local) as clocks:
         barrier(ws)
         torch.cuda.synchronize()
         e0.record(stream)
-        for t in range(W_steps, W_steps + K_steps):
-            mac.decode_step(*step_args(t), out=out, lse=lse)
-        mac.join()
+        if graph is not None:
+            graph.replay()
+        else:
+            for t in range(W_steps, W_steps + K_steps):
+                mac.decode_step(*step_args(t), out=out, lse=lse)
+            mac.join()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
@@ -285,13 +302,26 @@ def bench_ours(args, ws, rank, local):
     clk = clocks.summary()
     ms_max = max_over_ranks(ms, ws, dev)
     us_step = ms_max * 1e3 / K_steps
+    del graph
+
+    # the same K steps launched call by call from Python (host-bound when a
+    # step's GPU work is shorter than the launch path)
+    t_eager = W_steps + K_steps
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for t in range(t_eager, t_eager + K_steps):
+        mac.decode_step(*step_args(t), out=out, lse=lse)
+    mac.join()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_us = max_over_ranks(e0.elapsed_time(e1), ws, dev) * 1e3 / K_steps
 
     # per-kernel durations: the next K steps again with CUDA events around
     # every launch (on the stream each kernel runs on); these events sit
     # between the kernels, so this pass is kept out of the headline time
     mac.reset_stats()
     mac.set_profiling(True)
-    for t in range(W_steps + K_steps, W_steps + 2 * K_steps):
+    for t in range(W_steps + 2 * K_steps, W_steps + 3 * K_steps):
         mac.decode_step(*step_args(t), out=out, lse=lse)
     mac.join()
     torch.cuda.synchronize()
@@ -301,7 +331,7 @@ def bench_ours(args, ws, rank, local):
 
     # end to end through the C ABI with host (pinned) buffers
     pin = lambda x: x.cpu().pin_memory()
-    e2e_first = W_steps + 2 * K_steps
+    e2e_first = W_steps + 3 * K_steps
     h_in = {k: pin(inp[k][e2e_first:e2e_first + K_steps]) for k in ("q_pre", "q_post", "k_new", "v_new")}
     d_in = [torch.empty_like(inp[k][0]) for k in ("q_pre", "q_post", "k_new", "v_new")]
     h_out = torch.empty((B, H, cfg.head_dim), dtype=torch.bfloat16).pin_memory()
@@ -354,6 +384,9 @@ def bench_ours(args, ws, rank, local):
                    "accumulate": "fp32",
                    "l2": f"inputs larger than L2 (KV {B * Hkv * cfg.context * BYTES_PER_KV_TOKEN / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "timing": ("CUDA-graph replay of the K-step decode loop" if not args.eager else
+                   "per-call launches from Python"),
+        "eager_us_per_step": round(eager_us, 3),
         "tokens_per_s": round(sum_over_ranks(B, ws, dev) / (us_step * 1e-6), 1),
         "hbm_gbs_step": round(hbm_gbs, 1),
         "hbm_frac_of_8tbs": round(hbm_gbs / NOMINAL_HBM_GBS, 4),
@@ -615,6 +648,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time per-call launches instead of a CUDA-graph replay")
     ap.add_argument("--tau", type=float, default=None, help="threshold for the layer-stack workload (0.3 or 0.45)")
     ap.add_argument("--layers", type=int, default=48, help="layers of the stack workload")
     ap.add_argument("--sweep-contexts", default="4096,16384,65536,131072")

@@ -36,6 +36,12 @@
  *  - Errors: every call returns a mac_status; no exception or abort crosses
  *    the ABI.  A CUDA error is sticky: the handle returns MAC_ERR_CUDA from
  *    then on.  A handle is not thread-safe.
+ *  - Stream capture: the step calls enqueue only kernels (and, with
+ *    amend_band 1, event records and waits), so a decode loop can be
+ *    captured into a CUDA graph.  Call mac_sync before beginning a capture
+ *    and, with amend_band 1, mac_join on the capturing stream before ending
+ *    it.  Host-side length checks run at capture time: a replayed graph
+ *    advances the device state, not the checks.
  */
 #ifndef MAC_H
 #define MAC_H

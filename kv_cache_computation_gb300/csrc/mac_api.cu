@@ -137,6 +137,7 @@ struct mac_ctx {
     cudaStream_t side = nullptr;
     cudaEvent_t ev_complete = nullptr, ev_amend = nullptr;
     bool amend_pending = false;
+    unsigned long long amend_capture_id = 0;   // capture the outstanding Amend was recorded in (0: none)
     bool force_next = false;
     std::vector<int64_t> kv_len, steps, n_pages;
     mac_status sticky = MAC_OK;
@@ -188,6 +189,31 @@ mac_status check_handle(mac_ctx *h)
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+// Make stream s wait for the outstanding side-stream Amend.  During stream
+// capture the wait is legal only for an Amend recorded in the same capture;
+// one recorded before the capture began must already have been waited for
+// (mac_sync before capturing), so it is skipped.  *waited tells whether a
+// wait was enqueued.
+mac_status wait_amend(mac_ctx *h, cudaStream_t s, bool *waited)
+{
+    *waited = false;
+    if (!h->amend_pending) return MAC_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    unsigned long long id = 0;
+    MAC_CUDA(h, cudaStreamGetCaptureInfo(s, &cs, &id));
+    if (cs == cudaStreamCaptureStatusActive && id != h->amend_capture_id) return MAC_OK;
+    MAC_CUDA(h, cudaStreamWaitEvent(s, h->ev_amend, 0));
+    *waited = true;
+    return MAC_OK;
+}
+
+#define MAC_WAIT_AMEND(h, s)                                                \
+    do {                                                                    \
+        bool w_;                                                            \
+        mac_status st_ = wait_amend((h), (s), &w_);                         \
+        if (st_ != MAC_OK) return st_;                                      \
+    } while (0)
+
 int64_t capacity(const mac_ctx *h, int req)
 {
     int64_t cap = h->cfg.max_ctx;
@@ -238,7 +264,9 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
         if (h->kv_len[b] + 1 > capacity(h, b)) return MAC_ERR_CAPACITY;
 
     cudaStream_t s = (cudaStream_t)stream;
-    if (h->amend_pending) MAC_CUDA(h, cudaStreamWaitEvent(s, h->ev_amend, 0));
+    bool waited = false;
+    st = wait_amend(h, s, &waited);
+    if (st != MAC_OK) return st;
 
     StepArgs a{};
     a.batch = batch;
@@ -262,7 +290,6 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
     a.pdl = pe ? 0 : 1;
     // Match follows the previous step's combine directly in the stream only
     // when no side-stream Amend wait sits between them
-    const bool waited = h->amend_pending;
 
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[0], s));
     {
@@ -284,6 +311,10 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
         if (pe) MAC_CUDA(h, cudaEventRecord(pe[5], h->side));
         MAC_CUDA(h, cudaEventRecord(h->ev_amend, h->side));
         h->amend_pending = true;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        unsigned long long id = 0;
+        MAC_CUDA(h, cudaStreamGetCaptureInfo(h->side, &cs, &id));
+        h->amend_capture_id = cs == cudaStreamCaptureStatusActive ? id : 0;
     } else if (pe) {
         // Amend ran in the combine epilogue (or a full step has none): an
         // empty interval on the main stream
@@ -475,7 +506,7 @@ mac_status mac_set_page_table(mac_handle h, int req, const int32_t *dev_pages, i
     if (n_pages > 0 && !dev_pages) return MAC_ERR_INVALID_ARG;
     if ((int64_t)n_pages * kPage < h->kv_len[req]) return MAC_ERR_CAPACITY;
     cudaStream_t s = (cudaStream_t)stream;
-    if (h->amend_pending) MAC_CUDA(h, cudaStreamWaitEvent(s, h->ev_amend, 0));
+    MAC_WAIT_AMEND(h, s);
     if (n_pages > 0)
         MAC_CUDA(h, cudaMemcpyAsync(h->lay.page_table + (size_t)req * h->sz.pages_per_req, dev_pages,
                                     (size_t)n_pages * 4, cudaMemcpyDeviceToDevice, s));
@@ -492,7 +523,7 @@ mac_status mac_append_kv(mac_handle h, int req, const void *dev_k, const void *d
     if (!dev_k || !dev_v || !aligned16(dev_k) || !aligned16(dev_v)) return MAC_ERR_INVALID_ARG;
     if (h->kv_len[req] + n_tokens > capacity(h, req)) return MAC_ERR_CAPACITY;
     cudaStream_t s = (cudaStream_t)stream;
-    if (h->amend_pending) MAC_CUDA(h, cudaStreamWaitEvent(s, h->ev_amend, 0));
+    MAC_WAIT_AMEND(h, s);
     MAC_CUDA(h, launch_append(h->lay, req, (int)h->kv_len[req], (int)n_tokens, (const __nv_bfloat16 *)dev_k,
                               (const __nv_bfloat16 *)dev_v, s));
     h->kv_len[req] += n_tokens;
@@ -516,7 +547,7 @@ mac_status mac_join(mac_handle h, void *stream)
 {
     const mac_status st = check_handle(h);
     if (st != MAC_OK) return st;
-    if (h->amend_pending) MAC_CUDA(h, cudaStreamWaitEvent((cudaStream_t)stream, h->ev_amend, 0));
+    MAC_WAIT_AMEND(h, (cudaStream_t)stream);
     return MAC_OK;
 }
 
@@ -581,7 +612,7 @@ mac_status mac_reset_request(mac_handle h, int req, void *stream)
     if (st != MAC_OK) return st;
     if (req < 0 || req >= h->cfg.max_batch) return MAC_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    if (h->amend_pending) MAC_CUDA(h, cudaStreamWaitEvent(s, h->ev_amend, 0));
+    MAC_WAIT_AMEND(h, s);
     MAC_CUDA(h, cudaMemsetAsync(h->lay.ring_pos + (size_t)req * h->cfg.ring_len, 0, (size_t)h->cfg.ring_len * 4, s));
     MAC_CUDA(h, cudaMemsetAsync(h->lay.kv_len + req, 0, 4, s));
     MAC_CUDA(h, cudaMemsetAsync(h->lay.step_ctr + req, 0, 4, s));
@@ -625,7 +656,7 @@ mac_status mac_debug_force_decisions(mac_handle h, const int32_t *dev_slot, int 
     if (st != MAC_OK) return st;
     if (!dev_slot || batch < 1 || batch > h->cfg.max_batch) return MAC_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    if (h->amend_pending) MAC_CUDA(h, cudaStreamWaitEvent(s, h->ev_amend, 0));
+    MAC_WAIT_AMEND(h, s);
     MAC_CUDA(h, cudaMemcpyAsync(h->lay.forced_slot, dev_slot, (size_t)batch * h->cfg.heads * 4,
                                 cudaMemcpyDeviceToDevice, s));
     h->force_next = true;

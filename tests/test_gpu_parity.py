@@ -160,3 +160,39 @@ def test_plan_fits_one_wave_of_the_grid():
     st = p.mac.stats()
     grid = torch.cuda.get_device_properties(0).multi_processor_count * 2
     assert st["work_items"] / st["steps"] <= grid
+
+
+@pytest.mark.parametrize("amend_band", [0, 1])
+def test_graph_captured_decode_loop_matches_oracle(amend_band):
+    """A decode loop captured into a CUDA graph and replayed gives the same
+    per-step outputs as the oracle (mac_sync before capture, mac_join at its
+    end)."""
+    import numpy as np
+    from gpu_harness import check_out, KEYS
+    import oracle
+    c = cfg(steps=10, rho=0.995, ring_len=4, batch=2)
+    p = _pair(c, amend_band=amend_band)
+    for t in range(2):                           # eager steps first
+        p.mac_step(t, force=False, check_ring=False)
+    p.mac.sync()
+    B, H = c.batch, c.heads
+    ins = [[p.inputs[k][t].cuda().contiguous() for k in KEYS] for t in range(2, 10)]
+    outs = [torch.empty((B, H, 128), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    lses = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(8)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(8):
+                p.mac.decode_step(*ins[i], out=outs[i], lse=lses[i])
+            p.mac.join()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(8):
+        ref = p.orc.step(*[W.bf16_bits(p.inputs[k][i + 2]) for k in KEYS])
+        flag = oracle.decision_flags(ref["D"], ref["D2"], ref["qn2"], c.tau)
+        assert not flag.any()
+        check_out(outs[i], lses[i], ref, f"graph step {i}")
+    p.check_ring(9)
