@@ -41,7 +41,8 @@
  *    captured into a CUDA graph.  Call mac_sync before beginning a capture
  *    and, with amend_band 1, mac_join on the capturing stream before ending
  *    it.  Host-side length checks run at capture time: a replayed graph
- *    advances the device state, not the checks.
+ *    advances the device state, not the checks.  Calls made after a replay
+ *    must be ordered after it (same stream, or after synchronising).
  */
 #ifndef MAC_H
 #define MAC_H

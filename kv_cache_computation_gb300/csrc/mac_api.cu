@@ -202,6 +202,14 @@ mac_status wait_amend(mac_ctx *h, cudaStream_t s, bool *waited)
     unsigned long long id = 0;
     MAC_CUDA(h, cudaStreamGetCaptureInfo(s, &cs, &id));
     if (cs == cudaStreamCaptureStatusActive && id != h->amend_capture_id) return MAC_OK;
+    if (cs != cudaStreamCaptureStatusActive && h->amend_capture_id != 0) {
+        // the outstanding Amend belongs to a captured graph, which mac_join
+        // closed into the capturing stream: work ordered after its replay is
+        // already behind it, and the event cannot be waited on outside the graph
+        h->amend_pending = false;
+        h->amend_capture_id = 0;
+        return MAC_OK;
+    }
     MAC_CUDA(h, cudaStreamWaitEvent(s, h->ev_amend, 0));
     *waited = true;
     return MAC_OK;
@@ -555,6 +563,10 @@ mac_status mac_sync(mac_handle h, int timeout_ms)
 {
     const mac_status st = check_handle(h);
     if (st != MAC_OK) return st;
+    if (h->amend_pending && h->amend_capture_id != 0) {   // captured Amend: ordered by the graph's stream
+        h->amend_pending = false;
+        h->amend_capture_id = 0;
+    }
     if (h->amend_pending) {
         const auto t0 = std::chrono::steady_clock::now();
         for (;;) {

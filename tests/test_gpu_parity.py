@@ -170,7 +170,7 @@ def test_graph_captured_decode_loop_matches_oracle(amend_band):
     import numpy as np
     from gpu_harness import check_out, KEYS
     import oracle
-    c = cfg(steps=10, rho=0.995, ring_len=4, batch=2)
+    c = cfg(steps=11, rho=0.995, ring_len=4, batch=2)
     p = _pair(c, amend_band=amend_band)
     for t in range(2):                           # eager steps first
         p.mac_step(t, force=False, check_ring=False)
@@ -196,3 +196,7 @@ def test_graph_captured_decode_loop_matches_oracle(amend_band):
         assert not flag.any()
         check_out(outs[i], lses[i], ref, f"graph step {i}")
     p.check_ring(9)
+    # eager steps continue after the replay (ordered behind it on this stream)
+    out, lse = p.mac.decode_step(*[p.inputs[k][9].cuda().contiguous() for k in KEYS])
+    p.mac.sync()
+    assert out.isfinite().all()
