@@ -197,6 +197,6 @@ def test_graph_captured_decode_loop_matches_oracle(amend_band):
         check_out(outs[i], lses[i], ref, f"graph step {i}")
     p.check_ring(9)
     # eager steps continue after the replay (ordered behind it on this stream)
-    out, lse = p.mac.decode_step(*[p.inputs[k][9].cuda().contiguous() for k in KEYS])
+    out, lse = p.mac.decode_step(*[p.inputs[k][10].cuda().contiguous() for k in KEYS])
     p.mac.sync()
     assert out.isfinite().all()
