@@ -72,7 +72,9 @@ typedef struct {
     int kv_heads;       /* KV heads H_kv; heads % kv_heads == 0 and the group   */
                         /* G = heads / kv_heads is one of 1, 2, 4, 8, 16, 32     */
     int head_dim;       /* d; must be 128                                        */
-    int ring_len;       /* L: ring entries per (request, head), 1..64            */
+    int ring_len;       /* L: ring entries per (request, head), 1..4096; rings   */
+                        /* over 64 entries are scanned by a separate grid-wide  */
+                        /* kernel before Match decides                          */
     int band_r;         /* r: rectification band width in tokens, >= 1           */
     double tau;         /* L2 threshold, relative: hit iff                       */
                         /* ||q~_m - q~_e|| < tau * ||q~_m||; tau >= 0           */
@@ -179,6 +181,22 @@ mac_status mac_sync(mac_handle h, int timeout_ms);
 /* Copy the device counters out (waits for the device first). */
 mac_status mac_get_stats(mac_handle h, mac_stats *out);
 mac_status mac_reset_stats(mac_handle h);
+
+/* Seed request req's rings with n entries <q~, AS_{1:pos-r}> -- for example
+ * the last prefill queries and the summaries the caller's prefill attention
+ * produced -- so the first decode steps can already reuse them (the paper's
+ * 512-2048-entry match windows, Figure 6 and Tables 5 and 7, reach back into
+ * the prompt; the pages do not say how those entries are formed, so the
+ * caller supplies them).  dev_q_pre bf16 [n][heads][head_dim] (pre-RoPE),
+ * dev_o fp32 [n][heads][head_dim] (normalised output of AS_{1:pos-r}),
+ * dev_lse fp32 [n][heads] (its natural-log LSE; -inf for the empty set),
+ * host_pos int64 [n]: 1-based positions, strictly increasing, each <= the
+ * request's length.  Entries are inserted in order exactly as decode steps
+ * insert theirs (slot = step mod L, step + 1), so only the last L survive.
+ * Seed before decoding (positions must grow with insertion order).
+ * Synchronous (waits for stream). */
+mac_status mac_seed_ring(mac_handle h, int req, int n, const void *dev_q_pre, const float *dev_o,
+                         const float *dev_lse, const int64_t *host_pos, void *stream);
 
 /* Forget request req: length 0, empty rings, step counter 0.  Async on
  * stream (after outstanding Amend). */

@@ -55,6 +55,7 @@ SIGNATURES = {
     "mac_get_stats": (_i, [_vp, ctypes.POINTER(MacStats)]),
     "mac_reset_stats": (_i, [_vp]),
     "mac_reset_request": (_i, [_vp, _i, _vp]),
+    "mac_seed_ring": (_i, [_vp, _i, _i, _vp, _vp, _vp, _pi64, _vp]),
     "mac_set_profiling": (_i, [_vp, _i]),
     "mac_get_profile": (_i, [_vp, ctypes.POINTER(MacProfile)]),
     "mac_debug_force_decisions": (_i, [_vp, _vp, _i, _vp]),

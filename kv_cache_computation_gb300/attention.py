@@ -107,6 +107,18 @@ class MacAttention:
                N.lib().mac_append_kv(self._h, req, _dev(k, "k", torch.bfloat16, shape),
                                      _dev(v, "v", torch.bfloat16, shape), n, _stream_ptr(stream)), self._h)
 
+    def seed_ring(self, req: int, q_pre: torch.Tensor, o: torch.Tensor, lse: torch.Tensor, positions, stream=None):
+        """Insert ring entries <q~, AS_{1:pos-r}> (e.g. from the prefill) for request req."""
+        n = q_pre.shape[0]
+        pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+        if pos.shape != (n,):
+            raise ValueError("one position per entry")
+        _check("mac_seed_ring",
+               N.lib().mac_seed_ring(self._h, req, n, _dev(q_pre, "q_pre", torch.bfloat16, (n, self.heads, self.head_dim)),
+                                     _dev(o, "o", torch.float32, (n, self.heads, self.head_dim)),
+                                     _dev(lse, "lse", torch.float32, (n, self.heads)),
+                                     pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _stream_ptr(stream)), self._h)
+
     def reset_request(self, req: int, stream=None):
         _check("mac_reset_request", N.lib().mac_reset_request(self._h, req, _stream_ptr(stream)), self._h)
 

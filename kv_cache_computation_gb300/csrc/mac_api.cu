@@ -46,7 +46,7 @@ struct Sizes {
     int G = 0, pages_per_req = 0, num_pages = 0, ctx_stride = 0, item_cap = 0;
     size_t r_pos, r_q, r_o, r_lse;
     size_t s_page, s_kvlen, s_step, s_mcur, s_slot, s_own_slot, s_own_hit, s_dslot, s_dlo, s_dD, s_dqn2,
-        s_forced, s_qstash, s_glo, s_goff, s_items, s_nitems, s_po, s_pml, s_afo, s_afl, s_apo,
+        s_forced, s_dkey, s_seedpos, s_qstash, s_glo, s_goff, s_items, s_nitems, s_po, s_pml, s_afo, s_afl, s_apo,
         s_apl, s_stats, s_err;
 };
 
@@ -107,6 +107,8 @@ mac_status compute_sizes(const mac_config *c, Sizes *z)
     z->s_dD = s.take(BH * 4);
     z->s_dqn2 = s.take(BH * 4);
     z->s_forced = s.take(BH * 4);
+    z->s_dkey = s.take(BH * 8);
+    z->s_seedpos = s.take(L * 4);
     z->s_qstash = s.take(BH * kD * 2);
     z->s_glo = s.take(BG * 4);
     z->s_goff = s.take((BG + 1) * 4);
@@ -447,6 +449,8 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     L.dec_D = (float *)(sc + z.s_dD);
     L.dec_qn2 = (float *)(sc + z.s_dqn2);
     L.forced_slot = (int32_t *)(sc + z.s_forced);
+    L.dec_key = (unsigned long long *)(sc + z.s_dkey);
+    L.seed_pos = (int32_t *)(sc + z.s_seedpos);
     L.q_stash = (__nv_bfloat16 *)(sc + z.s_qstash);
     L.grp_lo = (int32_t *)(sc + z.s_glo);
     L.grp_item_off = (int32_t *)(sc + z.s_goff);
@@ -472,6 +476,8 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     if (e != cudaSuccess) return fail(e, "cudaMemset(scratch)");
     e = cudaMemset(rg + z.r_pos, 0, (size_t)cfg->max_batch * cfg->ring_len * 4);
     if (e != cudaSuccess) return fail(e, "cudaMemset(ring positions)");
+    e = cudaMemset(sc + z.s_dkey, 0xff, (size_t)cfg->max_batch * cfg->heads * 8);   // "no entry" keys
+    if (e != cudaSuccess) return fail(e, "cudaMemset(match keys)");
     int lo_prio = 0, hi_prio = 0;
     e = cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio);
     if (e != cudaSuccess) return fail(e, "cudaDeviceGetStreamPriorityRange");
@@ -630,6 +636,33 @@ mac_status mac_reset_request(mac_handle h, int req, void *stream)
     MAC_CUDA(h, cudaMemsetAsync(h->lay.step_ctr + req, 0, 4, s));
     h->kv_len[req] = 0;
     h->steps[req] = 0;
+    return MAC_OK;
+}
+
+mac_status mac_seed_ring(mac_handle h, int req, int n, const void *dev_q_pre, const float *dev_o,
+                         const float *dev_lse, const int64_t *host_pos, void *stream)
+{
+    const mac_status st = check_handle(h);
+    if (st != MAC_OK) return st;
+    if (req < 0 || req >= h->cfg.max_batch || n < 0) return MAC_ERR_INVALID_ARG;
+    if (n == 0) return MAC_OK;
+    if (!dev_q_pre || !dev_o || !dev_lse || !host_pos || !aligned16(dev_q_pre) || !aligned16(dev_o) ||
+        ((uintptr_t)dev_lse & 3))
+        return MAC_ERR_INVALID_ARG;
+    for (int i = 0; i < n; i++)
+        if (host_pos[i] < 1 || host_pos[i] > h->kv_len[req] || (i > 0 && host_pos[i] <= host_pos[i - 1]))
+            return MAC_ERR_INVALID_ARG;
+    const int L = h->cfg.ring_len;
+    const int first = n > L ? n - L : 0;   // only the last L entries survive the insertion
+    std::vector<int32_t> pos(n - first);
+    for (int i = first; i < n; i++) pos[i - first] = (int32_t)host_pos[i];
+    cudaStream_t s = (cudaStream_t)stream;
+    MAC_WAIT_AMEND(h, s);
+    MAC_CUDA(h, cudaMemcpyAsync(h->lay.seed_pos, pos.data(), pos.size() * 4, cudaMemcpyHostToDevice, s));
+    MAC_CUDA(h, launch_seed(h->lay, req, first, n, (int)h->steps[req], (const __nv_bfloat16 *)dev_q_pre, dev_o,
+                            dev_lse, s));
+    MAC_CUDA(h, cudaStreamSynchronize(s));   // the position staging buffer is reused by the next call
+    h->steps[req] += n;
     return MAC_OK;
 }
 

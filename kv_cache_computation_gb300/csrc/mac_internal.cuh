@@ -11,7 +11,9 @@ namespace macgpu {
 
 constexpr int kD = 128;                 // head_dim
 constexpr int kPage = 16;               // tokens per KV page / per staged block
-constexpr int kMaxRing = 64;            // ring entries per (request, head)
+constexpr int kMaxRing = 4096;          // ring entries per (request, head)
+constexpr int kSmallRing = 64;          // rings up to this size are scanned inside the Match kernel
+constexpr int kScanBlock = 256;         // ring entries per block of the wide-ring scan
 constexpr int kMaxGroup = 32;           // query heads per KV head
 constexpr int kMaxCtas = 1024;          // upper bound of the attention grid
 constexpr int kMaxGroupsPerStep = 1024; // max_batch * kv_heads (the plan is held in shared memory)
@@ -73,6 +75,8 @@ struct Layout {
     int32_t *dec_own_slot, *dec_own_hit, *dec_slot, *dec_lo;
     float *dec_D, *dec_qn2;
     int32_t *forced_slot;
+    unsigned long long *dec_key;   // [max_batch * H] wide rings: min over entries of (D bits << 32 | age)
+    int32_t *seed_pos;             // [L] positions of the entries a seeding call inserts
     __nv_bfloat16 *q_stash;   // [max_batch][H][D] post-RoPE query kept for Amend
 
     // plan
@@ -107,6 +111,8 @@ struct StepArgs {
 
 // launchers (mac_kernels.cu)
 cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_seed(const Layout &L, int req, int first, int n, int base_step, const __nv_bfloat16 *q,
+                        const float *o, const float *lse, cudaStream_t s);
 cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s);
 cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s);

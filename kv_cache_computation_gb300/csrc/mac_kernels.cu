@@ -350,7 +350,59 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
 // ring's loads are in flight at once; a warp argmin then picks the nearest
 // entry (ties to the larger position).
 // ---------------------------------------------------------------------------
-template <int MAX_THREADS>
+// ---------------------------------------------------------------------------
+// Wide rings (more than kSmallRing entries): every entry is one thread of a
+// (split, head, request) block; the block's best (distance, age) key goes
+// into dec_key with a 64-bit atomic minimum.  Distances are non-negative, so
+// their float bits order as unsigned integers; age 0 is the newest entry,
+// so equal distances resolve to the most recent position.
+// grid (ceil(L / kScanBlock), H, batch), block kScanBlock threads.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScanBlock) ring_scan_kernel(Layout L, StepArgs a)
+{
+    __shared__ __align__(16) uint4 sq[16];
+    __shared__ unsigned long long s_best;
+    pdl_launch_dependents();
+    pdl_wait();   // launched early behind the previous step: read nothing before its completion
+    const int h = blockIdx.y, b = blockIdx.z;
+    const size_t bh = (size_t)b * L.H + h;
+    if (threadIdx.x < 16) sq[threadIdx.x] = reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[threadIdx.x];
+    if (threadIdx.x == 0) s_best = ~0ull;
+    __syncthreads();
+    const int e = blockIdx.x * kScanBlock + threadIdx.x;
+    const int step = L.step_ctr[b];
+    if (e < L.ring_len) {
+        const int pe = L.ring_pos[(size_t)b * L.ring_len + e];
+        if (pe > 0) {
+            const uint4 *ent = reinterpret_cast<const uint4 *>(L.ring_q + (bh * L.ring_len + e) * kD);
+            uint4 c[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) c[i] = ent[i];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const uint4 qq = sq[i];
+                const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w}, ca[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[j]));
+                    const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ca[j]));
+                    const float d0 = qf.x - cf.x, d1 = qf.y - cf.y;
+                    acc[j] = fmaf(d0, d0, acc[j]);
+                    acc[j] = fmaf(d1, d1, acc[j]);
+                }
+            }
+            const float De = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            const int age = ((step - 1 - e) % L.ring_len + L.ring_len) % L.ring_len;
+            const unsigned long long key = ((unsigned long long)__float_as_uint(De) << 32) | (unsigned)age;
+            atomicMin(&s_best, key);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && s_best != ~0ull) atomicMin(&L.dec_key[bh], s_best);
+}
+
+template <int MAX_THREADS, bool WIDE>
 __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepArgs a)
 {
     __shared__ __align__(16) uint4 s_q[32][16];
@@ -373,7 +425,7 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
         // of the ring (position and query) and this head's queries.
         int pe0 = 0;
         uint4 c[16];
-        if (lane < L.ring_len) {
+        if (!WIDE && lane < L.ring_len) {
             pe0 = rpos[lane];
             const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)lane * kD);
 #pragma unroll
@@ -408,12 +460,22 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
         };
         int best = -1, best_pos = 0;
         float bestD = CUDART_INF_F;
-        if (pe0 > 0) {
+        if (WIDE) {   // the scan kernel left the best (distance, age) key
+            const unsigned long long key = L.dec_key[bh];
+            if (key != ~0ull) {
+                bestD = __uint_as_float((unsigned)(key >> 32));
+                const int age = (int)(key & 0xffffffffu);
+                best = ((L.step_ctr[b] - 1 - age) % L.ring_len + L.ring_len) % L.ring_len;
+                best_pos = rpos[best];
+            }
+            __syncwarp();
+            if (lane == 0) L.dec_key[bh] = ~0ull;   // ready for the next step
+        } else if (pe0 > 0) {
             best = lane;
             bestD = dist(c);
             best_pos = pe0;
         }
-        for (int e = lane + 32; e < L.ring_len; e += 32) {   // rings longer than a warp
+        for (int e = lane + 32; !WIDE && e < L.ring_len; e += 32) {   // rings longer than a warp
             const int pe = rpos[e];
             if (pe <= 0) continue;
             const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)e * kD);
@@ -427,7 +489,7 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
             }
         }
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
+        for (int o = 16; !WIDE && o; o >>= 1) {
             const float oD = __shfl_xor_sync(0xffffffffu, bestD, o);
             const int oe = __shfl_xor_sync(0xffffffffu, best, o);
             const int op = __shfl_xor_sync(0xffffffffu, best_pos, o);
@@ -1086,6 +1148,30 @@ __global__ void __launch_bounds__(1024) amend_kernel(Layout L, StepArgs a)
 }
 
 // ---------------------------------------------------------------------------
+// seed: entries first..n-1 of a seeding call into request req's rings, entry
+// i at slot (base_step + i) mod L, as if inserted by decode steps.  One warp
+// per (entry, head); q [n][H][D] bf16, o [n][H][D] fp32, lse [n][H] fp32.
+// ---------------------------------------------------------------------------
+__global__ void seed_kernel(Layout L, int req, int first, int n, int base_step, const __nv_bfloat16 *q,
+                            const float *o, const float *lse)
+{
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int i = first + gw / L.H, h = gw % L.H;
+    if (i >= n) return;
+    const int slot = (base_step + i) % L.ring_len;
+    const size_t src = (size_t)i * L.H + h;
+    const size_t e = ((size_t)req * L.H + h) * L.ring_len + slot;
+    if (lane < 16) reinterpret_cast<uint4 *>(L.ring_q + e * kD)[lane] = reinterpret_cast<const uint4 *>(q + src * kD)[lane];
+    reinterpret_cast<float4 *>(L.ring_o + e * kD)[lane] = reinterpret_cast<const float4 *>(o + src * kD)[lane];
+    if (lane == 0) {
+        L.ring_lse[e] = lse[src];
+        if (h == 0) L.ring_pos[(size_t)req * L.ring_len + slot] = L.seed_pos[i - first];
+        if (gw == 0) L.step_ctr[req] = base_step + n;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // append: n tokens of K and V [n][Hkv][D] at indices start.. of request req.
 // ---------------------------------------------------------------------------
 __global__ void append_kernel(Layout L, int req, int start, int n, const __nv_bfloat16 *k,
@@ -1171,8 +1257,23 @@ cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s
     // up to 16 heads per group: a 512-thread bound leaves room for the ring
     // entry held in registers during Match
     const dim3 grid(L.Hkv, a.batch), block(L.G * 32);
-    if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512>, grid, block, 0, s, a.pdl, L, a);
-    return launch_maybe_pdl(match_plan_kernel<1024>, grid, block, 0, s, a.pdl, L, a);
+    if (a.full_mode || L.ring_len <= kSmallRing) {
+        if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512, false>, grid, block, 0, s, a.pdl, L, a);
+        return launch_maybe_pdl(match_plan_kernel<1024, false>, grid, block, 0, s, a.pdl, L, a);
+    }
+    const dim3 sgrid((L.ring_len + kScanBlock - 1) / kScanBlock, L.H, a.batch);
+    cudaError_t e = launch_maybe_pdl(ring_scan_kernel, sgrid, dim3(kScanBlock), 0, s, a.pdl, L, a);
+    if (e != cudaSuccess) return e;
+    if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512, true>, grid, block, 0, s, a.pdl, L, a);
+    return launch_maybe_pdl(match_plan_kernel<1024, true>, grid, block, 0, s, a.pdl, L, a);
+}
+
+cudaError_t launch_seed(const Layout &L, int req, int first, int n, int base_step, const __nv_bfloat16 *q,
+                        const float *o, const float *lse, cudaStream_t s)
+{
+    const int warps = (n - first) * L.H;
+    seed_kernel<<<(warps + 7) / 8, 256, 0, s>>>(L, req, first, n, base_step, q, o, lse);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)

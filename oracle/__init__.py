@@ -73,6 +73,8 @@ def lib():
     L.orc_mac_step_heads.restype = ctypes.c_int
     L.orc_mac_step_heads.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16, _u16, _u16,
                                      _u16, _d, _d, _i32, _d, _d, _d, _i32, _i64]
+    L.orc_mac_seed.restype = ctypes.c_int
+    L.orc_mac_seed.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, _u16, _d, _d, _i64]
     L.orc_full_step.restype = ctypes.c_int
     L.orc_full_step.argtypes = [ctypes.c_void_p, ctypes.c_int, _u16, _u16, _u16, _d, _d]
     _lib = L
@@ -179,6 +181,18 @@ class MacState:
     def reset(self, b, kv_len):
         if lib().orc_mac_reset(self._h, b, kv_len) != 0:
             raise ValueError("bad request or length")
+
+    def seed(self, b, q_pre, o, lse, pos):
+        """Insert n ring entries for request b: q_pre uint16 [n, H, d], o
+        [n, H, d], lse [n, H], 1-based increasing positions [n]."""
+        q_pre = _u16c(q_pre)
+        o = np.ascontiguousarray(o, np.float64)
+        lse = np.ascontiguousarray(lse, np.float64)
+        pos = np.ascontiguousarray(pos, np.int64)
+        n = pos.shape[0]
+        assert q_pre.shape == (n, self.H, self.d) and o.shape == (n, self.H, self.d) and lse.shape == (n, self.H)
+        if lib().orc_mac_seed(self._h, b, n, _ptr(q_pre, _u16), _ptr(o, _d), _ptr(lse, _d), _ptr(pos, _i64)) != 0:
+            raise ValueError("bad seed entries")
 
     @property
     def direct_count(self):

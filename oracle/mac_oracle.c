@@ -283,6 +283,33 @@ void orc_mac_read_ring(const orc_mac *s, int64_t *pos, uint16_t *q, double *o, d
     if (step) memcpy(step, s->step, (size_t)s->B * sizeof(int64_t));
 }
 
+/* Seed request b's rings with n entries <q~, AS_{1:pos-r}> at 1-based
+ * positions pos[i] (strictly increasing, each <= kv_len[b]), inserted in
+ * order exactly as decode steps insert them: slot (step mod L), step + 1.
+ * q_pre [n][H][d] bf16 bits; o [n][H][d]; lse [n][H].  The pages do not say
+ * how prefill queries enter the rings; the caller supplies the entries (its
+ * prefill attention yields the summaries). */
+int orc_mac_seed(orc_mac *s, int b, int n, const uint16_t *q_pre, const double *o, const double *lse,
+                 const int64_t *pos)
+{
+    if (b < 0 || b >= s->B || n < 0) return -1;
+    for (int i = 0; i < n; i++)
+        if (pos[i] < 1 || pos[i] > s->kv_len[b] || (i > 0 && pos[i] <= pos[i - 1])) return -1;
+    const int H = s->H, d = s->d, L = s->L;
+    for (int i = 0; i < n; i++) {
+        const long slot = (long)(s->step[b] % L);
+        s->ring_pos[(long)b * L + slot] = pos[i];
+        for (int h = 0; h < H; h++) {
+            const long e = ((long)b * H + h) * L + slot;
+            memcpy(s->ring_q + e * d, q_pre + ((long)i * H + h) * d, (size_t)d * sizeof(uint16_t));
+            memcpy(s->ring_o + e * d, o + ((long)i * H + h) * d, (size_t)d * sizeof(double));
+            s->ring_lse[e] = lse[(long)i * H + h];
+        }
+        s->step[b] += 1;
+    }
+    return 0;
+}
+
 /* Append the new token's K and V at index kv_len[b] of each request. */
 static int append_new_token(orc_mac *s, int batch, const uint16_t *k_new, const uint16_t *v_new)
 {

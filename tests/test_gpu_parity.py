@@ -200,3 +200,48 @@ def test_graph_captured_decode_loop_matches_oracle(amend_band):
     out, lse = p.mac.decode_step(*[p.inputs[k][10].cuda().contiguous() for k in KEYS])
     p.mac.sync()
     assert out.isfinite().all()
+
+
+@pytest.mark.parametrize("ring_len,n_seed", [(128, 100), (1024, 1100)])
+def test_wide_ring_seeded_from_prefill(ring_len, n_seed):
+    """Rings far longer than a warp (scanned by the grid-wide kernel), seeded
+    with prefill entries: the last prefill queries of an AR(1) stream that
+    leads into the decode stream, with summaries AS_{1:pos-r} from the
+    oracle handed to both sides in fp32."""
+    import math
+    import numpy as np
+    import oracle
+    from conftest import bf16_value
+    c = cfg(ring_len=ring_len, steps=10, context=1500, rho=0.995, band_r=32, batch=2)
+    p = _pair(c)
+    B, H, d, G = c.batch, c.heads, c.head_dim, c.group
+    rng = np.random.default_rng(5)
+    # prefill queries: AR(1) run backwards from the first decode query
+    x = bf16_value(W.bf16_bits(p.inputs["q_pre"][0])).astype(np.float64)
+    seeds = np.empty((n_seed, B, H, d))
+    for i in range(n_seed - 1, -1, -1):
+        x = c.rho * x + math.sqrt(1 - c.rho ** 2) * rng.standard_normal(x.shape)
+        seeds[i] = x
+    pos = np.arange(c.context - n_seed + 1, c.context + 1, dtype=np.int64)
+    q_pre = torch.from_numpy(seeds).to(torch.bfloat16)
+    q_post = W.to_bf16(W.rope(q_pre.double().reshape(n_seed, B * H, d), torch.from_numpy(pos - 1), c.rope_base)
+                       ).reshape(n_seed, B, H, d)
+    for b in range(B):
+        qp = W.bf16_bits(q_pre[:, b].contiguous())
+        o = np.zeros((n_seed, H, d), np.float64)
+        lse = np.zeros((n_seed, H), np.float64)
+        for i in range(n_seed):
+            for h in range(H):
+                o[i, h], lse[i, h] = oracle.attention_summary(
+                    bf16_value(W.bf16_bits(q_post[i, b, h])), p.orc.K[b, :, h // G], p.orc.V[b, :, h // G],
+                    0, max(0, pos[i] - c.band_r), 1 / math.sqrt(d))
+        o32, l32 = o.astype(np.float32), lse.astype(np.float32)
+        p.orc.seed(b, qp, o32.astype(np.float64), l32.astype(np.float64), pos)
+        p.mac.seed_ring(b, q_pre[:, b].contiguous().cuda(), torch.from_numpy(o32).cuda(),
+                        torch.from_numpy(l32).cuda(), pos)
+    p.check_ring(-1)
+    hits = 0
+    for t in range(c.steps):
+        ref, _ = p.mac_step(t, force=True, check_ring=(t == c.steps - 1))
+        hits += int(ref["hit"].sum())
+    assert hits > 0

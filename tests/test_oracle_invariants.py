@@ -186,3 +186,48 @@ def test_kv_capacity_is_enforced(rng):
     kv = bits(np.zeros((c["B"], c["Hkv"], c["d"])))
     with pytest.raises(RuntimeError):
         mac.step(qp, qp, kv, kv)
+
+
+def test_seeded_ring_entries_are_matched_and_reused(rng):
+    """Entries seeded from prefill queries behave exactly like decode-step
+    entries: a later identical query reuses the seed's summary, and the output
+    is that summary merged with fresh band+tail attention."""
+    K, V, c = _setup(rng, ctx=300, steps=4, L=8, r=16, tau=0.05)
+    mac = oracle.MacState(K, V, c["H"], c["L"], c["r"], c["tau"])
+    s = 1 / math.sqrt(c["d"])
+    G = c["H"] // c["Hkv"]
+    for b in range(c["B"]):
+        mac.reset(b, c["ctx"])
+    n = 5
+    pos = np.array([200, 230, 260, 280, 299], np.int64)
+    qs = bits(rng.standard_normal((n, c["H"], c["d"])))
+    qpost = bits(rng.standard_normal((n, c["H"], c["d"])))
+    o = np.zeros((c["B"], n, c["H"], c["d"]))
+    lse = np.zeros((c["B"], n, c["H"]))
+    for b in range(c["B"]):
+        for i in range(n):
+            for h in range(c["H"]):
+                o[b, i, h], lse[b, i, h] = oracle.attention_summary(bf16_value(qpost[i, h]), K[b, :, h // G],
+                                                                    V[b, :, h // G], 0, pos[i] - c["r"], s)
+        mac.seed(b, qs, o[b], lse[b], pos)
+    ring = mac.ring()
+    assert (ring["step"] == n).all() and sorted(ring["pos"][0][ring["pos"][0] > 0].tolist()) == pos.tolist()
+    with pytest.raises(ValueError):
+        mac.seed(0, qs[:2], o[0, :2], lse[0, :2], np.array([5, 5], np.int64))      # not increasing
+    # a decode step whose pre- and post-RoPE queries equal seed 2's reuses it
+    shape = (c["B"], c["H"], c["d"])
+    kv = (c["B"], c["Hkv"], c["d"])
+    qp = np.broadcast_to(qs[2], shape).copy()
+    qq = np.broadcast_to(qpost[2], shape).copy()
+    out = mac.step(qp, qq, bits(rng.standard_normal(kv)), bits(rng.standard_normal(kv)))
+    assert out["hit"].all() and (out["p"] == pos[2]).all()
+    m = c["ctx"] + 1
+    for b in range(c["B"]):
+        for h in range(c["H"]):
+            tail = oracle.attention_summary(bf16_value(qq[b, h]), K[b, :, h // G], V[b, :, h // G],
+                                            pos[2] - c["r"], m, s)
+            o_ref, l_ref = oracle.merge(o[b, 2, h], lse[b, 2, h], *tail)
+            np.testing.assert_allclose(out["out"][b, h], o_ref, atol=1e-13)
+            # reusing an exact prefix summary with the same query is full attention
+            full = oracle.attention_summary(bf16_value(qq[b, h]), K[b, :, h // G], V[b, :, h // G], 0, m, s)
+            np.testing.assert_allclose(out["out"][b, h], full[0], atol=1e-12)
