@@ -75,7 +75,7 @@ def test_ring_layout_reproduces_table7():
 
 
 @pytest.mark.parametrize("bad", [dict(head_dim=64), dict(heads=24, kv_heads=8), dict(heads=30, kv_heads=8),
-                                 dict(ring_len=0), dict(ring_len=65), dict(band_r=0), dict(tau=-0.1),
+                                 dict(ring_len=0), dict(ring_len=4097), dict(band_r=0), dict(tau=-0.1),
                                  dict(tau=float("inf")), dict(max_batch=0), dict(max_ctx=0),
                                  dict(max_ctx=(1 << 30) + 1), dict(page_size=8), dict(plan_mode=2),
                                  dict(heads=64, kv_heads=1), dict(sm_scale=-1.0),
