@@ -5,7 +5,10 @@
 
 Workloads: gqa_128k_b1_hetero (default), gqa_32k_b8_paged, gqa_4k_b1_contig,
 qwen_stack_120k_b4 (48-layer stack, --tau 0.3|0.45), sweep (forced hit rate x
-context x batch, MQA and GQA; one JSON line per point).
+context x batch, MQA and GQA), match_windows (Match latency vs window and GQA
+setting), rectification (output error vs reuse gap and band; hit rate and
+skipped prefix vs threshold and window) -- the last three print one JSON line
+per point.
 
 A step is one MAC decode step (KV append, Match, planning, split-KV
 Complete, merge, Amend) for every request of the workload, on inputs already
@@ -611,6 +614,106 @@ def bench_sweep(args, ws, rank, local):
     return None
 
 
+def bench_match_windows(args, ws, rank, local):
+    """Match-stage latency against the window length L and the GQA setting
+    (analogue of the paper's Figure 8(a)): rings filled to L entries by
+    seeding, then K decode steps with per-phase events.  One JSON line per
+    point."""
+    from kv_cache_computation_gb300 import MacAttention
+    from kv_cache_computation_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ctx, steps, warm = 32768, args.steps, args.warmup
+    for kv in (1, 8):
+        for L in (16, 64, 256, 512, 1024, 2048):
+            cfg = W.DecodeConfig(f"match_window_gqa32x{kv}_ctx{ctx}_L{L}", 1, 32, kv, 128, ctx, warm + steps + 1, L, 64,
+                                 0.3, rho=0.95, paged=True, seed=20260331 + 6)
+            mac = MacAttention(32, kv, 128, L, 64, 0.3, max_batch=1, max_ctx=ctx + warm + steps + 8, page_size=16)
+            pt = W.page_tables(1, (ctx + warm + steps + 8 + 15) // 16, seed=cfg.seed).to(dev)
+            mac.set_page_table(0, pt[0].contiguous())
+            Kp, Vp = W.prefill_kv(cfg, device=dev)
+            mac.append_kv(0, Kp[0], Vp[0])
+            del Kp, Vp
+            # L prefill entries (query values only matter for the scan cost)
+            g = torch.Generator(device=dev)
+            g.manual_seed(L)
+            qs = torch.randn((L, 32, 128), generator=g, device=dev).to(torch.bfloat16)
+            o = torch.zeros((L, 32, 128), dtype=torch.float32, device=dev)
+            lse = torch.full((L, 32), -float("inf"), dtype=torch.float32, device=dev)
+            mac.seed_ring(0, qs, o, lse, list(range(ctx - L + 1, ctx + 1)))
+            inp = W.decode_inputs(cfg, device=dev)
+            step = lambda t: mac.decode_step(inp["q_pre"][t], inp["q_post"][t], inp["k_new"][t], inp["v_new"][t])
+            for t in range(warm):
+                step(t)
+            mac.sync()
+            mac.set_profiling(True)
+            for t in range(warm, warm + steps):
+                step(t)
+            mac.sync()
+            pr = mac.profile()
+            mac.set_profiling(False)
+            if rank == 0:
+                print(json.dumps({"workload": "match_window_sweep", "kind": "mqa" if kv == 1 else "gqa",
+                                  "heads": 32, "kv_heads": kv, "window": L, "context": ctx,
+                                  "match_us": round(pr["match_plan_ms"] * 1e3 / pr["steps"], 2),
+                                  "attention_us": round(pr["attention_ms"] * 1e3 / pr["steps"], 2)}), flush=True)
+            mac.close()
+    return None
+
+
+def bench_rectification(args, ws, rank, local):
+    """Synthetic analogue of the paper's Figures 4 and 5: on AR(1) query
+    streams, the MAC output against full attention (both on this GPU, same
+    inputs) by reuse gap and band width, and hit rate / skipped-prefix
+    fraction against the threshold and the window.  One JSON line per point."""
+    from kv_cache_computation_gb300 import MacAttention
+    from kv_cache_computation_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ctx, steps = 8192, args.steps
+    for rho in (0.95, 0.99):
+        for tau in (0.2, 0.3, 0.4, 0.5):
+            for L in (4, 16, 64):
+                for r in (16, 64, 256):
+                    cfg = W.DecodeConfig(f"rect_rho{rho}_tau{tau}_L{L}_r{r}", 1, 32, 8, 128, ctx, steps, L, r, tau,
+                                         rho=rho, paged=False, seed=20260331 + 7)
+                    mk = lambda: MacAttention(32, 8, 128, L, r, tau, max_batch=1, max_ctx=ctx + steps + 1, page_size=0)
+                    mac, full = mk(), mk()
+                    Kp, Vp = W.prefill_kv(cfg, device=dev)
+                    mac.append_kv(0, Kp[0], Vp[0])
+                    full.append_kv(0, Kp[0], Vp[0])
+                    inp = W.decode_inputs(cfg, device=dev)
+                    errs = {}
+                    hits = skipped = total = 0
+                    for t in range(steps):
+                        a = [inp[k][t] for k in ("q_pre", "q_post", "k_new", "v_new")]
+                        o_mac, _ = mac.decode_step(*a)
+                        o_full, _ = full.full_step(*a[1:])
+                        dec = mac.decisions(1)
+                        pos = mac.read_ring(0)["pos"] if dec["hit"].any() else None
+                        e = ((o_mac.float() - o_full.float()).abs().amax(-1) /
+                             o_full.float().abs().amax(-1)).cpu().numpy()[0]
+                        m = ctx + t + 1
+                        for h in range(32):
+                            total += 1
+                            if dec["hit"][0, h]:
+                                hits += 1
+                                p = int(pos[dec["slot"][0, h]]) if pos is not None else m
+                                gap = m - p
+                                skipped += max(0, p - r)
+                                errs.setdefault(gap, []).append(float(e[h]))
+                    mac.close()
+                    full.close()
+                    if rank == 0:
+                        print(json.dumps({"workload": "rectification_study", "rho": rho, "tau": tau, "window": L,
+                                          "band_r": r, "context": ctx, "steps": steps,
+                                          "hit_rate": round(hits / total, 4),
+                                          "skipped_prefix_fraction": round(skipped / (total * (ctx + steps / 2)), 4),
+                                          "error_by_gap": {str(k): [round(float(np.mean(v)), 6), len(v)]
+                                                           for k, v in sorted(errs.items())}}), flush=True)
+    return None
+
+
 def bench_reference(args, ws, rank, local):
     """The fp64 oracle on the host cores (rank 0 only)."""
     if rank != 0:
@@ -665,6 +768,10 @@ def main():
         res = bench_stack(args, ws, rank, local)
     elif args.workload == "sweep":
         res = bench_sweep(args, ws, rank, local)
+    elif args.workload == "match_windows":
+        res = bench_match_windows(args, ws, rank, local)
+    elif args.workload == "rectification":
+        res = bench_rectification(args, ws, rank, local)
     else:
         res = bench_ours(args, ws, rank, local)
     if rank == 0 and res is not None:
