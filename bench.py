@@ -549,11 +549,26 @@ def bench_sweep(args, ws, rank, local):
     kvs = [int(x) for x in args.sweep_kv_heads.split(",")]
 
     def timed(fn, t0, n):
+        """us per step of fn(t0..t0+n-1): captured into a CUDA graph and
+        replayed (per-call launches with --eager)."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        g = None
+        if not args.eager:
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    for t in range(t0, t0 + n):
+                        fn(t)
+            torch.cuda.synchronize()
         e0.record(stream)
-        for t in range(t0, t0 + n):
-            fn(t)
+        if g is not None:
+            g.replay()
+        else:
+            for t in range(t0, t0 + n):
+                fn(t)
         e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / n
