@@ -244,10 +244,93 @@ __device__ __forceinline__ int plan_chunk(const Layout &L, const StepArgs &a, co
     return max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
 }
 
+// Up to 32 groups: one warp plans alone -- lane g holds group g, 32 chunk
+// candidates are counted at once (lane k counts candidate k), a ballot picks
+// the smallest that fits, a shuffle scan gives the offsets.
+__device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &ps)
+{
+    const int nbg = a.batch * L.Hkv;
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = 0, sp = 0;
+    if (lane < nbg) {
+        hi = __ldcg(&L.m_cur[lane / L.Hkv]);
+        lo = __ldcg(&L.grp_lo[lane]);
+        sp = plan_split(L, a, lo, hi);
+    }
+    long long T = lane < nbg ? hi - lo : 0, Tf = lane < nbg ? hi : 0;
+    int nseg = lane < nbg ? (sp > lo) + (hi > sp) : 0;
+    for (int o = 16; o; o >>= 1) {
+        T += __shfl_xor_sync(0xffffffffu, T, o);
+        Tf += __shfl_xor_sync(0xffffffffu, Tf, o);
+    }
+    nseg = warp_sum_int(nseg);
+    int C = kMinChunk;
+    if (a.plan_mode == 0) {
+        const long long P = a.grid_ctas;
+        long long Q = (4ll * nseg <= P) ? P : P * (1 + (2ll * nseg + P - 1) / P);
+        if (Q > L.item_cap) Q = L.item_cap;
+        long long c_lo = round_up16((T + Q - 1) / Q);
+        long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg)) : (1ll << 30);
+        if (c_lo < kMinChunk) c_lo = kMinChunk;
+        if (c_hi < c_lo) c_hi = c_lo;
+        // candidates c_lo + 16 * stride * k, k = 0..31 (the last one is c_hi)
+        for (;;) {
+            const long long span16 = (c_hi - c_lo) / 16;
+            const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
+            long long cand = c_lo + 16 * stride * lane;
+            if (cand > c_hi) cand = c_hi;
+            int cnt = 0;
+            for (int g = 0; g < nbg; g++) {
+                const int glo = __shfl_sync(0xffffffffu, lo, g), ghi = __shfl_sync(0xffffffffu, hi, g);
+                const int gsp = __shfl_sync(0xffffffffu, sp, g);
+                cnt += n_chunks(glo, gsp, (int)cand) + n_chunks(gsp, ghi, (int)cand);
+            }
+            const unsigned fit = __ballot_sync(0xffffffffu, cnt <= Q);
+            const int k = fit ? __ffs(fit) - 1 : 31;
+            const long long ck = __shfl_sync(0xffffffffu, cand, k);
+            if (stride == 1 || k == 0) {
+                c_hi = ck;
+                break;
+            }
+            c_hi = ck;   // refine between the previous candidate and this one
+            c_lo = __shfl_sync(0xffffffffu, cand, k - 1) + 16;
+        }
+        C = (int)c_hi;
+    }
+    // per-group counts and offsets
+    const int Cg = a.plan_mode == 0 ? C : (lane < nbg ? plan_chunk(L, a, ps, nbg, lo, hi) : kMinChunk);
+    const int cnt = lane < nbg ? n_chunks(lo, sp, Cg) + n_chunks(sp, hi, Cg) : 0;
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, x, 31);
+    if (lane < nbg) {
+        ps.lo[lane] = lo;
+        ps.hi[lane] = hi;
+        ps.off[lane] = x - cnt;
+    }
+    if (lane == 0) {
+        ps.off[nbg] = total;
+        ps.total = total < L.item_cap ? total : L.item_cap;
+        ps.C = C;
+        ps.T = T;
+        ps.Tf = Tf;
+    }
+    return true;
+}
+
 __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
 {
     const int nbg = a.batch * L.Hkv;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (nbg <= 32) {
+        if (w == 0) cta_plan_small(L, a, ps);
+        __syncthreads();
+        return;
+    }
     for (int bg = threadIdx.x; bg < nbg; bg += blockDim.x) {
         ps.hi[bg] = __ldcg(&L.m_cur[bg / L.Hkv]);   // m: the length after this step's append
         ps.lo[bg] = __ldcg(&L.grp_lo[bg]);
