@@ -31,6 +31,10 @@ constexpr int kMaxGroupsPerStep = 1024; // max_batch * kv_heads (the plan is hel
 constexpr int kAttnWarps = MAC_ATTN_WARPS;         // warps per attention CTA
 constexpr int kAttnStages = MAC_ATTN_STAGES;       // pipeline stages per page lane
 constexpr int kPrefetchAhead = MAC_PREFETCH_AHEAD; // pages per lane prefetched into L2 past the copy front
+#ifndef MAC_SPECULATIVE_PAGES
+#define MAC_SPECULATIVE_PAGES 4
+#endif
+constexpr int kSpeculativePages = MAC_SPECULATIVE_PAGES;  // pages per lane of the previous step's item warmed in L2
 constexpr int kStageBytes = 2 * kPage * kD * 2;   // one K page + one V page (bf16): 8 KB
 constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
 constexpr int kMinChunk = 64;           // smallest work-item span in tokens

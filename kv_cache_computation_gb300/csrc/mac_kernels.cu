@@ -691,6 +691,25 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 
     __shared__ PlanShared ps;
     pdl_launch_dependents();
+    // While Match runs, HBM is idle: warm L2 with the first pages of the item
+    // this CTA streamed in the previous step (consecutive steps plan almost
+    // alike).  Only a hint: every index is bounds-checked, so a stale or
+    // unrelated entry costs bandwidth, never correctness.
+    if (kSpeculativePages > 0 && gtid == 0 && blockIdx.x < L.item_cap) {
+        const int4 prev = L.items[blockIdx.x];
+        const int pb = prev.x / L.Hkv, pgrp = prev.x - pb * L.Hkv;
+        if (prev.x >= 0 && pb < L.max_batch && prev.y >= 0 && prev.y < prev.z) {
+            for (int k = 0; k < kSpeculativePages; k++) {
+                const int pg = (prev.y >> 4) + pl + k * NP;
+                if (pg * 16 >= prev.z) break;
+                bool ok = true;
+                const size_t off = kv_block(L, pb, pgrp, pg, ok);
+                if (!ok) break;
+                prefetch_l2_bulk(L.k_pool + off, 4096);
+                prefetch_l2_bulk(L.v_pool + off, 4096);
+            }
+        }
+    }
     pdl_wait();   // spans come from match_plan
     cta_plan(L, a, ps);
     const int nbg = a.batch * L.Hkv;
