@@ -156,6 +156,24 @@ __device__ __forceinline__ int n_chunks(int a, int b, int C)
     return b > a ? (b - 1) / C - a / C + 1 : 0;
 }
 
+// Division by a chunk size C shared by many dividends: R = ceil(2^64 / C)
+// once, then floor(x / C) is the high word of x R.  For 0 <= x < 2^31 and
+// 2 <= C < 2^33, x R / 2^64 exceeds x / C by less than 2^-33 while the
+// fractional part of x / C is at most 1 - 1/C, so the floor is exact
+// (division by invariant integers using multiplication, Granlund and
+// Montgomery 1994).
+__device__ __forceinline__ unsigned long long recip_ceil(int C) { return ~0ull / (unsigned long long)C + 1ull; }
+
+__device__ __forceinline__ int div_r(int x, unsigned long long R)
+{
+    return (int)__umul64hi((unsigned long long)(unsigned)x, R);
+}
+
+__device__ __forceinline__ int n_chunks_r(int a, int b, unsigned long long R)
+{
+    return b > a ? div_r(b - 1, R) - div_r(a, R) + 1 : 0;
+}
+
 // x rounded up to a multiple of 16, clamped to 2^30 (the longest request)
 __device__ __forceinline__ int round_up16(long long x)
 {
@@ -229,6 +247,7 @@ struct PlanShared {
     int C;
     int total;
     long long T, Tf;
+    unsigned long long R;   // recip_ceil(C) (balanced mode)
 };
 
 __device__ __forceinline__ int plan_split(const Layout &L, const StepArgs &a, int lo, int hi)
@@ -264,13 +283,24 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
         Tf += __shfl_xor_sync(0xffffffffu, Tf, o);
     }
     nseg = warp_sum_int(nseg);
+    if (lane < nbg) {
+        ps.lo[lane] = lo;
+        ps.hi[lane] = hi;
+    }
+    __syncwarp();
     int C = kMinChunk;
+    unsigned long long RC = 0;
     if (a.plan_mode == 0) {
-        const long long P = a.grid_ctas;
-        long long Q = (4ll * nseg <= P) ? P : P * (1 + (2ll * nseg + P - 1) / P);
+        const int P = a.grid_ctas;
+        int Q = (4 * nseg <= P) ? P : P * (1 + (2 * nseg + P - 1) / P);
         if (Q > L.item_cap) Q = L.item_cap;
-        long long c_lo = round_up16((T + Q - 1) / Q);
-        long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg)) : (1ll << 30);
+        // The smallest fitting chunk is at least T / Q (count(C) >= T / C)
+        // and at most T / (Q - 2 nseg) (count(C) < T / C + 2 nseg).  Float
+        // quotients (relative error < 2^-22) widened by 2^-20 bracket both.
+        const float Tq = (float)T;
+        long long c_lo = (long long)(Tq / (float)Q * (1.f - 0x1p-20f)) / 16 * 16;
+        long long c_hi = Q > 2 * nseg ? round_up16((long long)(Tq / (float)(Q - 2 * nseg) * (1.f + 0x1p-20f)) + 16)
+                                      : (1ll << 30);
         if (c_lo < kMinChunk) c_lo = kMinChunk;
         if (c_hi < c_lo) c_hi = c_lo;
         // candidates c_lo + 16 * stride * k, k = 0..31 (the last one is c_hi)
@@ -279,17 +309,19 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
             const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
             long long cand = c_lo + 16 * stride * lane;
             if (cand > c_hi) cand = c_hi;
+            const unsigned long long R = recip_ceil((int)cand);
             int cnt = 0;
+#pragma unroll 4
             for (int g = 0; g < nbg; g++) {
-                const int glo = __shfl_sync(0xffffffffu, lo, g), ghi = __shfl_sync(0xffffffffu, hi, g);
-                const int gsp = __shfl_sync(0xffffffffu, sp, g);
-                cnt += n_chunks(glo, gsp, (int)cand) + n_chunks(gsp, ghi, (int)cand);
+                const int glo = ps.lo[g], ghi = ps.hi[g], gsp = plan_split(L, a, glo, ghi);
+                cnt += n_chunks_r(glo, gsp, R) + n_chunks_r(gsp, ghi, R);
             }
             const unsigned fit = __ballot_sync(0xffffffffu, cnt <= Q);
             const int k = fit ? __ffs(fit) - 1 : 31;
             const long long ck = __shfl_sync(0xffffffffu, cand, k);
             if (stride == 1 || k == 0) {
                 c_hi = ck;
+                RC = __shfl_sync(0xffffffffu, R, k);
                 break;
             }
             c_hi = ck;   // refine between the previous candidate and this one
@@ -298,8 +330,15 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
         C = (int)c_hi;
     }
     // per-group counts and offsets
-    const int Cg = a.plan_mode == 0 ? C : (lane < nbg ? plan_chunk(L, a, ps, nbg, lo, hi) : kMinChunk);
-    const int cnt = lane < nbg ? n_chunks(lo, sp, Cg) + n_chunks(sp, hi, Cg) : 0;
+    int cnt = 0;
+    if (lane < nbg) {
+        if (a.plan_mode == 0) {
+            cnt = n_chunks_r(lo, sp, RC) + n_chunks_r(sp, hi, RC);
+        } else {
+            const int Cg = plan_chunk(L, a, ps, nbg, lo, hi);
+            cnt = n_chunks(lo, sp, Cg) + n_chunks(sp, hi, Cg);
+        }
+    }
     int x = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -307,15 +346,12 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
         if (lane >= o) x += y;
     }
     const int total = __shfl_sync(0xffffffffu, x, 31);
-    if (lane < nbg) {
-        ps.lo[lane] = lo;
-        ps.hi[lane] = hi;
-        ps.off[lane] = x - cnt;
-    }
+    if (lane < nbg) ps.off[lane] = x - cnt;
     if (lane == 0) {
         ps.off[nbg] = total;
         ps.total = total < L.item_cap ? total : L.item_cap;
         ps.C = C;
+        ps.R = RC;
         ps.T = T;
         ps.Tf = Tf;
     }
@@ -353,10 +389,11 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
         int C = kMinChunk;
         if (a.plan_mode == 0) {
             auto count = [&](int Cc) {
+                const unsigned long long R = recip_ceil(Cc);
                 int c = 0;
                 for (int bg = lane; bg < nbg; bg += 32) {
                     const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
-                    c += n_chunks(lo, sp, Cc) + n_chunks(sp, hi, Cc);
+                    c += n_chunks_r(lo, sp, R) + n_chunks_r(sp, hi, R);
                 }
                 return warp_sum_int(c);
             };
@@ -378,6 +415,7 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
         }
         if (lane == 0) {
             ps.C = C;
+            ps.R = recip_ceil(C);
             ps.T = T;
             ps.Tf = Tf;
         }
@@ -390,8 +428,12 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
         int cnt = 0;
         if (bg < nbg) {
             const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
-            const int C = plan_chunk(L, a, ps, nbg, lo, hi);
-            cnt = n_chunks(lo, sp, C) + n_chunks(sp, hi, C);
+            if (a.plan_mode == 0) {
+                cnt = n_chunks_r(lo, sp, ps.R) + n_chunks_r(sp, hi, ps.R);
+            } else {
+                const int C = plan_chunk(L, a, ps, nbg, lo, hi);
+                cnt = n_chunks(lo, sp, C) + n_chunks(sp, hi, C);
+            }
         }
         int tot;
         const int off = base + block_exclusive_scan(cnt, &tot);
@@ -417,12 +459,13 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
     const int bg = g0, k = it - ps.off[bg];
     const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
     const int C = plan_chunk(L, a, ps, nbg, lo, hi);
-    const int nA = n_chunks(lo, sp, C);
+    const unsigned long long R = a.plan_mode == 0 ? ps.R : recip_ceil(C);
+    const int nA = n_chunks_r(lo, sp, R);
     if (k < nA) {
-        const int c = lo / C + k;
+        const int c = div_r(lo, R) + k;
         return make_int4(bg, max(lo, c * C), min(sp, (c + 1) * C), 0);
     }
-    const int c = sp / C + (k - nA);
+    const int c = div_r(sp, R) + (k - nA);
     return make_int4(bg, max(sp, c * C), min(hi, (c + 1) * C), 1);
 }
 
@@ -689,16 +732,44 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // K tile row (token) this lane addresses
     const int vtok = (lane & 7) + 8 * (lane >> 4);         // V tile row (token) this lane addresses
 
+    // Q^T fragments of group bg (head column 8 ht + r4) and the band+tail
+    // starts dec_lo of this thread's two head columns (8 ht + 2 c4, + 1).
+    auto load_group = [&](int bg, uint32_t (&qf)[8][2], int &d0, int &d1) {
+        const int b = bg / L.Hkv, g = bg - b * L.Hkv;
+        const size_t hrow = (size_t)b * L.H + (size_t)g * G;
+        const int hn = 8 * ht + r4;
+        if (hn < G) {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.q_post + (hrow + hn) * kD);
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {
+                qf[kk][0] = qrow[8 * kk + c4];
+                qf[kk][1] = qrow[8 * kk + 4 + c4];
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) qf[kk][0] = qf[kk][1] = 0u;
+        }
+        const int hc0 = 8 * ht + 2 * c4;
+        d0 = hc0 < G ? L.dec_lo[hrow + hc0] : 0;
+        d1 = hc0 + 1 < G ? L.dec_lo[hrow + hc0 + 1] : 0;
+    };
+
     __shared__ PlanShared ps;
     pdl_launch_dependents();
-    // While Match runs, HBM is idle: warm L2 with the first pages of the item
-    // this CTA streamed in the previous step (consecutive steps plan almost
-    // alike).  Only a hint: every index is bounds-checked, so a stale or
-    // unrelated entry costs bandwidth, never correctness.
-    if (kSpeculativePages > 0 && gtid == 0 && blockIdx.x < L.item_cap) {
+    // Consecutive steps plan almost alike, so this CTA's first item is
+    // likely the one it had in the previous step (a hint only: a stale or
+    // unrelated entry costs bandwidth, never correctness).
+    int spec_bg = -1;
+    if (blockIdx.x < L.item_cap) {
+        const int4 prev = L.items[blockIdx.x];
+        if (prev.x >= 0 && prev.x < a.batch * L.Hkv && prev.y >= 0 && prev.y < prev.z) spec_bg = prev.x;
+    }
+    // While Match runs, HBM is idle: warm L2 with the first pages of that
+    // item (every index is bounds-checked).
+    if (kSpeculativePages > 0 && gtid == 0 && spec_bg >= 0) {
         const int4 prev = L.items[blockIdx.x];
         const int pb = prev.x / L.Hkv, pgrp = prev.x - pb * L.Hkv;
-        if (prev.x >= 0 && pb < L.max_batch && prev.y >= 0 && prev.y < prev.z) {
+        {
             for (int k = 0; k < kSpeculativePages; k++) {
                 const int pg = (prev.y >> 4) + pl + k * NP;
                 if (pg * 16 >= prev.z) break;
@@ -711,6 +782,10 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         }
     }
     pdl_wait();   // spans come from match_plan
+    // the likely first item's queries load while the plan is made
+    uint32_t q_spec[8][2];
+    int d0_spec = 0, d1_spec = 0;
+    if (spec_bg >= 0) load_group(spec_bg, q_spec, d0_spec, d1_spec);
     cta_plan(L, a, ps);
     const int nbg = a.batch * L.Hkv;
     const int n_items = ps.total;
@@ -735,27 +810,23 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 
         // Q^T fragments for head column n = r4 of this tile
         uint32_t qf[8][2];
-        {
-            const int hn = 8 * ht + r4;
-            if (hn < G) {
-                const uint32_t *qrow =
-                    reinterpret_cast<const uint32_t *>(a.q_post + ((size_t)b * L.H + (size_t)g * G + hn) * kD);
+        int d0, d1;
+        if (it == (int)blockIdx.x && bg == spec_bg) {
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) {
-                    qf[kk][0] = qrow[8 * kk + c4];
-                    qf[kk][1] = qrow[8 * kk + 4 + c4];
-                }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < 8; kk++) qf[kk][0] = qf[kk][1] = 0u;
+            for (int kk = 0; kk < 8; kk++) {
+                qf[kk][0] = q_spec[kk][0];
+                qf[kk][1] = q_spec[kk][1];
             }
+            d0 = d0_spec;
+            d1 = d1_spec;
+        } else {
+            load_group(bg, qf, d0, d1);
         }
         // this thread's two head columns and their first valid token (columns
         // past the group's heads are computed and discarded: no mask)
         const int hc0 = 8 * ht + 2 * c4, hc1 = hc0 + 1;
-        const size_t hrow = (size_t)b * L.H + (size_t)g * G;
-        const int lo0 = hc0 < G ? max(ilo, L.dec_lo[hrow + hc0]) : ilo;
-        const int lo1 = hc1 < G ? max(ilo, L.dec_lo[hrow + hc1]) : ilo;
+        const int lo0 = max(ilo, d0);
+        const int lo1 = max(ilo, d1);
         const int lo_max = max(lo0, lo1);
 
         float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
