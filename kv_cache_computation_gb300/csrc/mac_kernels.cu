@@ -1430,10 +1430,10 @@ cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s
     // up to 16 heads per group: a 512-thread bound leaves room for the ring
     // entry held in registers during Match
     const dim3 grid(L.Hkv, a.batch), block(L.G * 32);
-    if (a.full_mode || (L.ring_len <= kSmallRing && L.G <= 16)) {
-        if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512, false>, grid, block, 0, s, a.pdl, L, a);
-        return launch_maybe_pdl(match_plan_kernel<1024, false>, grid, block, 0, s, a.pdl, L, a);
-    }
+    if (L.G <= 16 && (a.full_mode || L.ring_len <= kSmallRing))
+        return launch_maybe_pdl(match_plan_kernel<512, false>, grid, block, 0, s, a.pdl, L, a);
+    if (a.full_mode)   // no ring work: the wide instantiation only appends and plans
+        return launch_maybe_pdl(match_plan_kernel<1024, true>, grid, block, 0, s, a.pdl, L, a);
     const dim3 sgrid((L.ring_len + kScanBlock - 1) / kScanBlock, L.H, a.batch);
     cudaError_t e = launch_maybe_pdl(ring_scan_kernel, sgrid, dim3(kScanBlock), 0, s, a.pdl, L, a);
     if (e != cudaSuccess) return e;
