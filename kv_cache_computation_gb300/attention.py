@@ -132,7 +132,8 @@ class MacAttention:
         return out, lse, lp
 
     def decode_step(self, q_pre, q_post, k_new, v_new, out=None, lse=None, want_lse=True, stream=None):
-        """One MAC decode step (Match, Complete; Amend on the side stream)."""
+        """One MAC decode step: Match, Complete, merge and Amend (Amend on the side
+        stream when the handle was made with amend_band=1)."""
         B = q_pre.shape[0]
         qs, ks = (B, self.heads, self.head_dim), (B, self.kv_heads, self.head_dim)
         out, lse, lp = self._outs(B, q_pre.device, out, lse, want_lse)
