@@ -192,12 +192,14 @@ def run_oracle(cfg, K_dev, V_dev, inp, budget_s, max_steps, fixed_steps=None, wa
 
     Calibrates on one whole step, then times either ``fixed_steps`` steps
     (each a sample of query heads sized so the run fits ``budget_s``) or as
-    many whole steps as fit ``budget_s`` (2 .. max_steps).  Returns (us per
-    whole step, OpenMP threads, description of the sample)."""
+    many whole steps as fit ``budget_s`` (2 .. max_steps).  Then one
+    full-attention step on all cores and one MAC step on a single core (a
+    head sample, scaled).  Returns (us per whole step, OpenMP threads,
+    description of the sample, dict of the extra timings and the CPU model)."""
     import oracle
     from kv_cache_computation_gb300 import workloads as W
     B, H = cfg.batch, cfg.heads
-    n_need = warm + 1 + (fixed_steps if fixed_steps else max_steps)
+    n_need = warm + 3 + (fixed_steps if fixed_steps else max_steps)   # + the full-attention and one-core steps
     t_max = cfg.context + n_need + 1
     Ko = np.zeros((B, t_max, cfg.kv_heads, cfg.head_dim), np.uint16)
     Vo = np.zeros_like(Ko)
@@ -233,7 +235,44 @@ def run_oracle(cfg, K_dev, V_dev, inp, budget_s, max_steps, fixed_steps=None, wa
               + ("" if heads == H else f", query heads 0..{heads - 1} of {H} per step, scaled x{H // heads} "
                                        "to a whole step")
               + f"; {el:.1f} s of CPU time")
-    return us, oracle.num_threads(), sample
+    threads = oracle.num_threads()
+    extra = {"cpu_model": cpu_model()}
+    # full attention (every head over the whole context), one step on all cores
+    t0 = time.perf_counter()
+    st.full_step(*host_inputs(inp, t)[1:])
+    extra["full_attention_us_per_step"] = round((time.perf_counter() - t0) * 1e6, 1)
+    t += 1
+    # one core: one MAC step over a sample of heads, scaled
+    h1 = max(1, H // 16)
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        st.step(*host_inputs(inp, t), heads=(0, h1))
+        extra["single_core_us_per_step"] = round((time.perf_counter() - t0) * 1e6 * H / h1, 1)
+        extra["single_core_sample"] = f"one decode step, query heads 0..{h1 - 1} of {H}, scaled x{H // h1}"
+    finally:
+        oracle.set_num_threads(threads)
+    return us, threads, sample, extra
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def bench_ours(args, ws, rank, local):
@@ -417,9 +456,9 @@ def bench_ours(args, ws, rank, local):
     }
     mac.sync()
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        us, cores, sample = run_oracle(cfg, Kp, Vp, inp, args.cpu_budget, max_steps=min(K_steps, 256))
+        us, cores, sample, extra = run_oracle(cfg, Kp, Vp, inp, args.cpu_budget, max_steps=min(K_steps, 256))
         result["cpu_baseline"] = {"value": round(us, 1), "unit": "us/step", "cores": cores, "kind": "oracle",
-                                  "sample": sample}
+                                  "sample": sample, **extra}
     mac.close()
     return result
 
@@ -739,8 +778,8 @@ def bench_reference(args, ws, rank, local):
     cfg = workload(args.workload, args.band_r, W_steps + K_steps + 4)
     Kp, Vp = W.prefill_kv(cfg)
     inp = W.decode_inputs(cfg)
-    us, cores, sample = run_oracle(cfg, Kp, Vp, inp, args.ref_budget, max_steps=K_steps, fixed_steps=K_steps,
-                                   warm=W_steps)
+    us, cores, sample, extra = run_oracle(cfg, Kp, Vp, inp, args.ref_budget, max_steps=K_steps,
+                                          fixed_steps=K_steps, warm=W_steps)
     return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": ws,
             "steps": K_steps, "warmup": W_steps, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -748,7 +787,7 @@ def bench_reference(args, ws, rank, local):
                        "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "ring_len": cfg.ring_len,
                        "band_r": cfg.band_r, "tau": cfg.tau},
             "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **extra},
             "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

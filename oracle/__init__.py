@@ -44,6 +44,8 @@ def lib():
     L.orc_bf16_to_double.restype = ctypes.c_double
     L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
     L.orc_num_threads.restype = ctypes.c_int
+    L.orc_set_num_threads.restype = None
+    L.orc_set_num_threads.argtypes = [ctypes.c_int]
     L.orc_attention_summary.restype = None
     L.orc_attention_summary.argtypes = [_d, _u16, _u16, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                         ctypes.c_int, ctypes.c_double, _d, _d]
@@ -84,6 +86,11 @@ def lib():
 def num_threads() -> int:
     """OpenMP threads the oracle's parallel loops use."""
     return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's following parallel loops."""
+    lib().orc_set_num_threads(int(n))
 
 
 def _u16c(a):

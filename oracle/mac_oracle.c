@@ -76,6 +76,16 @@ int orc_num_threads(void)
 #endif
 }
 
+/* Threads for the following parallel loops (timing runs on fewer cores).   */
+void orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* Attention summary AS_S(q) over S = [lo, hi) of one (request, kv-head).    */
 /*   z_j = scale * <q, k_j>,  lse = log sum_j exp(z_j),                      */
