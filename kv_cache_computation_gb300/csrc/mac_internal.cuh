@@ -36,6 +36,13 @@ constexpr int kPrefetchAhead = MAC_PREFETCH_AHEAD; // pages per lane prefetched 
 #endif
 constexpr int kSpeculativePages = MAC_SPECULATIVE_PAGES;  // pages per lane of the previous step's item warmed in L2
 constexpr int kStageBytes = 2 * kPage * kD * 2;   // one K page + one V page (bf16): 8 KB
+#ifndef MAC_ATTN_CUDA_CORE
+#define MAC_ATTN_CUDA_CORE 0
+#endif
+// Comparison build: the page contractions S^T = K Q^T and O^T += V^T P^T on
+// fp32 FMA instead of mma.sync (same tiles, same layouts, q staged in shared
+// memory); selected at compile time, never at run time.
+constexpr bool kAttnCudaCore = MAC_ATTN_CUDA_CORE != 0;
 constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
 constexpr int kMinChunk = 64;           // smallest work-item span in tokens
 constexpr int kPlanCache = 1024;        // groups the planner caches in shared memory

@@ -225,6 +225,17 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// acc += a . b over 8 bf16 pairs (4 words each), in fp32 (comparison build)
+__device__ __forceinline__ void dot8_bf16(float &acc, uint4 a, uint4 b)
+{
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[i] & 0xffff0000u), __uint_as_float(bw[i] & 0xffff0000u), acc);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Planning (prologue of every attention CTA; all CTAs derive the same plan).
 // Per (request, kv-head) group the streamed span is [lo_g, m), lo_g being the
@@ -715,6 +726,8 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     const int ht = warp % NH, pl = warp / NH;
     const int gtid = threadIdx.x - pl * GT;
     uint8_t *lane_smem = smem + (size_t)pl * S * kStageBytes;
+    // comparison build only: the query rows of the head tiles, past the stages and the lane-merge area
+    uint8_t *q_tiles = smem + max((size_t)NP * S * kStageBytes, (size_t)NP * G * kD * 4 + (size_t)NP * G * 8);
     const uint32_t lane_smem_u32 = smem_u32(lane_smem);
     const int r4 = lane >> 2, c4 = lane & 3;
     const float sl2 = L.scale_log2;
@@ -822,6 +835,17 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         } else {
             load_group(bg, qf, d0, d1);
         }
+        if constexpr (kAttnCudaCore) {   // the item's query rows (bf16), 8 per head tile, zeros past G
+            __syncthreads();
+            for (int i = threadIdx.x; i < NH * 8 * 16; i += NW * 32) {
+                const int hh = i >> 4, ch = i & 15;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (hh < G)
+                    v = reinterpret_cast<const uint4 *>(a.q_post + ((size_t)b * L.H + (size_t)g * G + hh) * kD)[ch];
+                reinterpret_cast<uint4 *>(q_tiles)[i] = v;
+            }
+            __syncthreads();
+        }
         // this thread's two head columns and their first valid token (columns
         // past the group's heads are computed and discarded: no mask)
         const int hc0 = 8 * ht + 2 * c4, hc1 = hc0 + 1;
@@ -886,7 +910,22 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 
             // S^T = K Q^T
             float s[4] = {0.f, 0.f, 0.f, 0.f};
-            {
+            if constexpr (kAttnCudaCore) {
+                const uint8_t *Kp = lane_smem + (k % S) * kStageBytes;
+                const uint8_t *qa = q_tiles + (size_t)(8 * ht + 2 * c4) * 256, *qb = qa + 256;
+                const int ra = r4, rb = r4 + 8;
+#pragma unroll 4
+                for (int ch = 0; ch < 16; ch++) {
+                    const uint4 ka = *reinterpret_cast<const uint4 *>(Kp + ra * 256 + ((ch ^ (ra & 7)) << 4));
+                    const uint4 kb = *reinterpret_cast<const uint4 *>(Kp + rb * 256 + ((ch ^ (rb & 7)) << 4));
+                    const uint4 q0 = *reinterpret_cast<const uint4 *>(qa + ch * 16);
+                    const uint4 q1 = *reinterpret_cast<const uint4 *>(qb + ch * 16);
+                    dot8_bf16(s[0], ka, q0);
+                    dot8_bf16(s[1], ka, q1);
+                    dot8_bf16(s[2], kb, q0);
+                    dot8_bf16(s[3], kb, q1);
+                }
+            } else {
                 const uint32_t rbase = Ks + krow * 256;
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++) {
@@ -933,6 +972,28 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             l1 += p1 + p3;
             m0 = mn0;
             m1 = mn1;
+            if constexpr (kAttnCudaCore) {   // O^T += V^T P^T with fp32 P gathered from the lanes that hold it
+                const uint8_t *Vp = lane_smem + (k % S) * kStageBytes + 4096;
+#pragma unroll 2
+                for (int t = 0; t < 16; t++) {
+                    const int src = (t & 7) * 4 + c4;
+                    const float pa = __shfl_sync(0xffffffffu, t < 8 ? p0 : p2, src);
+                    const float pb = __shfl_sync(0xffffffffu, t < 8 ? p1 : p3, src);
+                    const uint8_t *vrow = Vp + t * 256 + r4 * 2;
+#pragma unroll
+                    for (int mt = 0; mt < 8; mt++) {
+                        const float v0 = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(
+                                                             vrow + (((2 * mt) ^ (t & 7)) << 4)) << 16);
+                        const float v1 = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(
+                                                             vrow + (((2 * mt + 1) ^ (t & 7)) << 4)) << 16);
+                        acc[mt][0] = fmaf(v0, pa, acc[mt][0]);
+                        acc[mt][1] = fmaf(v0, pb, acc[mt][1]);
+                        acc[mt][2] = fmaf(v1, pa, acc[mt][2]);
+                        acc[mt][3] = fmaf(v1, pb, acc[mt][3]);
+                    }
+                }
+                continue;
+            }
             // P^T fragments (hi + lo bf16 parts) via in-register transpose
             const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
             const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
@@ -1384,7 +1445,8 @@ static size_t attention_smem(int G)
     const int NH = head_tiles(G), NP = kAttnWarps / NH;
     const size_t pipe = (size_t)NP * kAttnStages * kStageBytes;
     const size_t red = (size_t)NP * G * kD * 4 + (size_t)NP * G * 8;
-    return pipe > red ? pipe : red;
+    const size_t q_tiles = kAttnCudaCore ? (size_t)NH * 8 * kD * 2 : 0;   // after the stages
+    return (pipe > red ? pipe : red) + q_tiles;
 }
 
 template <int NH>
