@@ -129,3 +129,66 @@ class Pair:
                 e = rel_err(go[~empty], lo[~empty])
                 assert e.max() <= OUT_TOL, f"step {t} ring o error {e.max():.3g}"
                 assert np.abs(gl[~empty] - ll[~empty]).max() <= LSE_TOL, f"step {t} ring lse error"
+
+
+class SampledPair:
+    """A MAC handle over a whole large workload (all requests, KV generated on
+    the GPU) and the oracle over a sample of its requests.  Requests are
+    independent, so every output, decision and ring of a sampled request must
+    match; the GPU makes its own decisions (forced-hit streams keep every
+    distance far from the threshold)."""
+
+    def __init__(self, cfg: W.DecodeConfig, requests, page_size=16):
+        self.cfg, self.sel = cfg, list(requests)
+        B, dev = cfg.batch, torch.device("cuda")
+        self.t_max = cfg.context + cfg.steps
+        K, V = W.prefill_kv(cfg, device=dev)
+        self.mac = MacAttention(cfg.heads, cfg.kv_heads, cfg.head_dim, cfg.ring_len, cfg.band_r, cfg.tau,
+                                max_batch=B, max_ctx=self.t_max, page_size=page_size)
+        if page_size:
+            pages = W.page_tables(B, (self.t_max + 15) // 16, seed=cfg.seed).cuda()
+            for b in range(B):
+                self.mac.set_page_table(b, pages[b].contiguous())
+        for b in range(B):
+            self.mac.append_kv(b, K[b], V[b])
+        n = len(self.sel)
+        Ko = np.zeros((n, self.t_max, cfg.kv_heads, cfg.head_dim), np.uint16)
+        Vo = np.zeros_like(Ko)
+        for i, b in enumerate(self.sel):
+            Ko[i, :cfg.context] = W.bf16_bits(K[b])
+            Vo[i, :cfg.context] = W.bf16_bits(V[b])
+        del K, V
+        torch.cuda.empty_cache()
+        self.orc = oracle.MacState(Ko, Vo, cfg.heads, cfg.ring_len, cfg.band_r, cfg.tau)
+        for i in range(n):
+            self.orc.reset(i, cfg.context)
+        self.inputs = W.decode_inputs(cfg, device=dev)
+        self.hits = 0
+
+    def step(self, t, check_ring=False):
+        dev = [self.inputs[k][t].contiguous() for k in KEYS]
+        out, lse = self.mac.decode_step(*dev)
+        host = [W.bf16_bits(x[self.sel]) for x in dev]
+        ref = self.orc.step(*host)
+        self.mac.sync()
+        dec = self.mac.decisions(self.cfg.batch)
+        flag = oracle.decision_flags(ref["D"], ref["D2"], ref["qn2"], self.cfg.tau)
+        hit, slot = dec["hit"][self.sel], dec["slot"][self.sel]
+        # a flagged near-tie may pick another entry, but only for a miss: a
+        # forced hit's entry is 100x nearer than any other
+        ok = (hit == ref["hit"]) & ((slot == ref["slot"]) | (flag & ~ref["hit"].astype(bool)))
+        assert ok.all(), f"step {t}: decisions differ at {np.argwhere(~ok)[:5].tolist()}"
+        self.hits += int(ref["hit"].sum())
+        check_out(out[self.sel], lse[self.sel], ref, f"step {t}")
+        if check_ring:
+            ring = self.orc.ring()
+            for i, b in enumerate(self.sel):
+                g = self.mac.read_ring(b)
+                np.testing.assert_array_equal(g["pos"], ring["pos"][i])
+                valid = ring["pos"][i] > 0
+                np.testing.assert_array_equal(g["q"][:, valid], ring["q"][i][:, valid])
+                live = ring["lse"][i][:, valid] != -np.inf
+                if live.any():
+                    e = rel_err(g["o"][:, valid][live], ring["o"][i][:, valid][live])
+                    assert e.max() <= OUT_TOL, f"step {t} ring o error {e.max():.3g}"
+        return ref

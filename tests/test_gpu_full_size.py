@@ -53,3 +53,25 @@ def test_llama_128k_heterogeneous_rho(band_r):
     p, hits = _run(cfg, 24, page_size=16, ring_every=12)
     # per-head rho ~ U[0.5, 0.99]: only the most correlated heads hit
     assert hits > 0
+
+
+def test_qwen_stack_layer_4x120k_hits():
+    """One layer of the 48-layer stack at full size (4 x 122880, 32 q / 4 KV
+    heads, per-channel K/V scales), tau 0.45 so heads hit and miss."""
+    cfg = W.qwen_moe_stack_120k_b4(steps=12, tau=0.45, layers=1)
+    p, hits = _run(cfg, 12, page_size=16, ring_every=6)
+    assert hits > 0
+
+
+@pytest.mark.parametrize("kv_heads", [8, 1])
+def test_forced_hit_sweep_largest_point(kv_heads):
+    """The sweep's largest points, 32 requests x 131072 tokens (GQA 32/8,
+    17 GB of KV; MQA 32/1), 90 % forced hits, every request on the GPU and
+    four of them (the first and last two) on the oracle."""
+    from gpu_harness import SampledPair
+    cfg = W.sweep_point(131072, 32, 0.9, kv_heads, steps=6)
+    p = SampledPair(cfg, requests=[0, 1, 30, 31])
+    for t in range(cfg.steps):
+        p.step(t, check_ring=(t == cfg.steps - 1))
+    assert p.hits > 0
+    assert p.mac.stats()["device_error"] == 0
