@@ -1080,7 +1080,6 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 // AS_{1:m-r} = AS_{1:m} (-) band, and the ring insert.  With amend_band 1 the
 // summaries are handed to the side-stream Amend kernel instead.
 // ---------------------------------------------------------------------------
-constexpr int kCombineWarps = 8;
 
 __device__ __forceinline__ void fma4(float4 &acc, float w, float4 v)
 {
@@ -1115,6 +1114,11 @@ __device__ __forceinline__ bool remove_band(float lf, float4 of, float lb, float
     return false;
 }
 
+// KB partials per warp per round of loads: 4, or 16 when a group may hold
+// hundreds of items (one request's single KV group spread over the grid).
+constexpr int kCombineWarps = 8;
+
+template <int KB>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, StepArgs a)
 {
     __shared__ float s_red[2][kCombineWarps];
@@ -1153,7 +1157,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
         lp = 1.f;
         op = o_ring;
     }
-    constexpr int kBatch = 4;
+    constexpr int kBatch = KB;
     for (int i0 = off0 + w; i0 < off1; i0 += kBatch * kCombineWarps) {
         float2 ml[kBatch];
         int sg[kBatch];
@@ -1523,7 +1527,12 @@ cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cu
 
 cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    return launch_maybe_pdl(combine_kernel, dim3(a.batch * L.H), dim3(kCombineWarps * 32), 0, s, a.pdl != 0, L, a);
+    // a group holds at most about grid / groups + 2 items
+    const int nbg = a.batch * L.Hkv;
+    const int per_group = (a.grid_ctas + nbg - 1) / nbg + 2;
+    const dim3 grid(a.batch * L.H), block(kCombineWarps * 32);
+    if (per_group > 128) return launch_maybe_pdl(combine_kernel<16>, grid, block, 0, s, a.pdl != 0, L, a);
+    return launch_maybe_pdl(combine_kernel<4>, grid, block, 0, s, a.pdl != 0, L, a);
 }
 
 static size_t amend_smem(int G) { return (size_t)2 * kBandTile * kBandRow + (size_t)G * kD * 2; }
