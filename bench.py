@@ -371,29 +371,81 @@ def bench_ours(args, ws, rank, local):
     mac.set_profiling(False)
     st_p = mac.stats()
 
-    # end to end through the C ABI with host (pinned) buffers
-    pin = lambda x: x.cpu().pin_memory()
+    # end to end through the C ABI with host (pinned) buffers: every step one
+    # host-to-device copy of its packed inputs and one device-to-host copy of
+    # its packed result (out, then lse).  The copies run on a second stream,
+    # double-buffered: step i + 1's inputs travel while step i computes, and
+    # step i's result returns while step i + 1 computes.
+    keys = ("q_pre", "q_post", "k_new", "v_new")
     e2e_first = W_steps + 3 * K_steps
-    h_in = {k: pin(inp[k][e2e_first:e2e_first + K_steps]) for k in ("q_pre", "q_post", "k_new", "v_new")}
-    d_in = [torch.empty_like(inp[k][0]) for k in ("q_pre", "q_post", "k_new", "v_new")]
-    h_out = torch.empty((B, H, cfg.head_dim), dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    sizes = [inp[k][0].numel() for k in keys]
+    offs = [sum(sizes[:i]) for i in range(len(keys))]
+    h_pack = torch.empty((K_steps, sum(sizes)), dtype=torch.bfloat16).pin_memory()
+    for i in range(K_steps):
+        for k, o, n in zip(keys, offs, sizes):
+            h_pack[i, o:o + n] = inp[k][e2e_first + i].reshape(-1).cpu()
+    n_out, n_lse = B * H * cfg.head_dim * 2, B * H * 4
+    d_pack = [torch.empty(sum(sizes), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    d_in = [[p[o:o + n].view(inp[k][0].shape) for k, o, n in zip(keys, offs, sizes)] for p in d_pack]
+    d_res = [torch.empty(n_out + n_lse, dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_e = [r[:n_out].view(torch.bfloat16).view(B, H, cfg.head_dim) for r in d_res]
+    lse_e = [r[n_out:].view(torch.float32).view(B, H) for r in d_res]
+    h_res = torch.empty((K_steps, n_out + n_lse), dtype=torch.uint8).pin_memory()
+    cs = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of the buffer's next step have arrived
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # the buffer's step has finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # the buffer's result has been read back
+
+    def e2e_loop(main):
+        cs.wait_stream(main)
+        with torch.cuda.stream(cs):
+            d_pack[0].copy_(h_pack[0], non_blocking=True)
+            ev_in[0].record(cs)
+        for i in range(K_steps):
+            j = i & 1
+            if i + 1 < K_steps:
+                with torch.cuda.stream(cs):
+                    if i >= 1:
+                        cs.wait_event(ev_done[j ^ 1])   # step i - 1 has consumed that buffer
+                    d_pack[j ^ 1].copy_(h_pack[i + 1], non_blocking=True)
+                    ev_in[j ^ 1].record(cs)
+            main.wait_event(ev_in[j])
+            if i >= 2:
+                main.wait_event(ev_out[j])   # step i - 2's result has left that buffer
+            mac.decode_step(*d_in[j], out=out_e[j], lse=lse_e[j], stream=main)
+            ev_done[j].record(main)
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_done[j])
+                h_res[i].copy_(d_res[j], non_blocking=True)
+                ev_out[j].record(cs)
+        mac.join(stream=main)
+        main.wait_stream(cs)
+
+    # like the headline: the loop captured once into a CUDA graph (copies
+    # included) and replayed; --eager issues it call by call
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                e2e_loop(cap)
+        torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2.record(stream)
-    for i in range(K_steps):
-        for d, k in zip(d_in, ("q_pre", "q_post", "k_new", "v_new")):
-            d.copy_(h_in[k][i], non_blocking=True)
-        mac.decode_step(*d_in, out=out, lse=lse)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
-    mac.join()
+    if graph is not None:
+        graph.replay()
+    else:
+        e2e_loop(stream)
     e3.record(stream)
     torch.cuda.synchronize()
+    del graph
     e2e_us = max_over_ranks(e2.elapsed_time(e3), ws, dev) * 1e3 / K_steps
-    h2d = sum(x[0].numel() * x.element_size() for x in h_in.values())
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    h2d = sum(sizes) * 2
+    d2h = n_out + n_lse
 
     # bytes
     kv_read = st["kv_tokens_read"] * BYTES_PER_KV_TOKEN
