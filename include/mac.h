@@ -109,10 +109,13 @@ typedef struct {
 
 /* Accumulated GPU time per phase since profiling was enabled (ms). */
 typedef struct {
-    double match_plan_ms;     /* KV append + Match + planning kernel            */
-    double attention_ms;      /* split-KV band+tail / full attention kernel     */
-    double combine_ms;        /* log-domain merge kernel                        */
-    double amend_ms;          /* Amend kernel (side stream)                     */
+    double match_plan_ms;     /* KV append + Match (+ the ring scan of long     */
+                              /* rings)                                         */
+    double attention_ms;      /* work plan + split-KV band+tail / full          */
+                              /* attention kernel                               */
+    double combine_ms;        /* log-domain merge kernel (with Amend's removal  */
+                              /* and ring insert when amend_band is 0)          */
+    double amend_ms;          /* Amend kernel (side stream, amend_band 1)       */
     uint64_t steps;           /* steps timed                                    */
 } mac_profile;
 
