@@ -75,3 +75,40 @@ def test_forced_hit_sweep_largest_point(kv_heads):
         p.step(t, check_ring=(t == cfg.steps - 1))
     assert p.hits > 0
     assert p.mac.stats()["device_error"] == 0
+
+
+def test_llama_128k_graph_replay_like_the_benchmark():
+    """The benchmark's headline path at its full size: the decode loop of the
+    128K workload captured into a CUDA graph and replayed, the GPU making its
+    own decisions; every replayed step equals the oracle's."""
+    import oracle
+    from gpu_harness import Pair, check_out, KEYS
+    cfg = W.llama_gqa_128k_b1_hetero(steps=14, band_r=64)
+    p = Pair(cfg, page_size=16)
+    for t in range(4):                           # eager steps first
+        p.mac_step(t, force=False, check_ring=False)
+    p.mac.sync()
+    B, H, n = cfg.batch, cfg.heads, 10
+    ins = [[p.inputs[k][t].cuda().contiguous() for k in KEYS] for t in range(4, 4 + n)]
+    outs = [torch.empty((B, H, 128), dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    lses = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(n)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                p.mac.decode_step(*ins[i], out=outs[i], lse=lses[i])
+            p.mac.join()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    hits = 0
+    for i in range(n):
+        ref = p.orc.step(*[W.bf16_bits(p.inputs[k][4 + i]) for k in KEYS])
+        assert not oracle.decision_flags(ref["D"], ref["D2"], ref["qn2"], cfg.tau).any()
+        hits += int(ref["hit"].sum())
+        check_out(outs[i], lses[i], ref, f"graph step {i}")
+    p.check_ring(4 + n - 1)
+    assert hits > 0
+    assert p.mac.stats()["device_error"] == 0
