@@ -46,7 +46,7 @@ struct Sizes {
     int G = 0, pages_per_req = 0, num_pages = 0, ctx_stride = 0, item_cap = 0;
     size_t r_pos, r_q, r_o, r_lse;
     size_t s_page, s_kvlen, s_step, s_mcur, s_slot, s_own_slot, s_own_hit, s_dslot, s_dlo, s_dD, s_dqn2,
-        s_forced, s_dkey, s_seedpos, s_qstash, s_glo, s_goff, s_items, s_nitems, s_po, s_pml, s_afo, s_afl, s_apo,
+        s_forced, s_dkey, s_seedpos, s_qstash, s_glo, s_segc, s_goff, s_items, s_nitems, s_po, s_pml, s_afo, s_afl, s_apo,
         s_apl, s_stats, s_err;
 };
 
@@ -111,6 +111,7 @@ mac_status compute_sizes(const mac_config *c, Sizes *z)
     z->s_seedpos = s.take(L * 4);
     z->s_qstash = s.take(BH * kD * 2);
     z->s_glo = s.take(BG * 4);
+    z->s_segc = s.take(BG * 2 * 4);
     z->s_goff = s.take((BG + 1) * 4);
     z->s_items = s.take(cap * sizeof(int4));
     z->s_nitems = s.take(4);
@@ -453,6 +454,7 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     L.seed_pos = (int32_t *)(sc + z.s_seedpos);
     L.q_stash = (__nv_bfloat16 *)(sc + z.s_qstash);
     L.grp_lo = (int32_t *)(sc + z.s_glo);
+    L.seg_claim = (int32_t *)(sc + z.s_segc);
     L.grp_item_off = (int32_t *)(sc + z.s_goff);
     L.items = (int4 *)(sc + z.s_items);
     L.n_items = (int32_t *)(sc + z.s_nitems);

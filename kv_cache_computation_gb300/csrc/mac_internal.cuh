@@ -36,6 +36,13 @@ constexpr int kPrefetchAhead = MAC_PREFETCH_AHEAD; // pages per lane prefetched 
 #endif
 constexpr int kSpeculativePages = MAC_SPECULATIVE_PAGES;  // pages per lane of the previous step's item warmed in L2
 constexpr int kStageBytes = 2 * kPage * kD * 2;   // one K page + one V page (bf16): 8 KB
+#ifndef MAC_DYN_FRAC
+#define MAC_DYN_FRAC 10
+#endif
+// A work item of at least kDynMinPages pages leaves its last npg * kDynFrac /
+// 128 pages (at least 2) to its segment's shared pool; 0 turns pools off.
+constexpr int kDynFrac = MAC_DYN_FRAC;
+constexpr int kDynMinPages = 32;
 #ifndef MAC_ATTN_CUDA_CORE
 #define MAC_ATTN_CUDA_CORE 0
 #endif
@@ -93,6 +100,7 @@ struct Layout {
 
     // plan
     int32_t *grp_lo;          // [max_batch * Hkv] first token any head of the group reads
+    int32_t *seg_claim;       // [max_batch * Hkv * 2] pool pages claimed per group segment this step
     int32_t *grp_item_off;    // [max_batch * Hkv + 1]
     int4 *items;              // [item_cap] {b*Hkv+g, lo, hi, segment}
     int32_t *n_items;

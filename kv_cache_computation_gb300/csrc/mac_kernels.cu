@@ -768,6 +768,7 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     };
 
     __shared__ PlanShared ps;
+    __shared__ int s_pool[NP][8];   // per page lane: pool pages claimed, by lane step past its own pages
     pdl_launch_dependents();
     // Consecutive steps plan almost alike, so this CTA's first item is
     // likely the one it had in the previous step (a hint only: a stale or
@@ -846,11 +847,15 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             }
             __syncthreads();
         }
+        // the item's segment of the group, [slo, shi): any page of it may be
+        // computed here (see the pool below), so masks use its bounds
+        const int glo = ps.lo[bg], ghi = ps.hi[bg], gsp = plan_split(L, a, glo, ghi);
+        const int slo = item.w ? gsp : glo, shi = item.w ? ghi : gsp;
         // this thread's two head columns and their first valid token (columns
         // past the group's heads are computed and discarded: no mask)
         const int hc0 = 8 * ht + 2 * c4, hc1 = hc0 + 1;
-        const int lo0 = max(ilo, d0);
-        const int lo1 = max(ilo, d1);
+        const int lo0 = max(slo, d0);
+        const int lo1 = max(slo, d1);
         const int lo_max = max(lo0, lo1);
 
         float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
@@ -860,7 +865,58 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 
         const int pg0 = ilo >> 4, pg1 = (ihi - 1) >> 4;
         const int npg = pg1 - pg0 + 1;
-        const int npl = pl < npg ? (npg - pl + NP - 1) / NP : 0;
+
+        // Pages.  Every long item of the segment keeps its last ~8 % of pages
+        // back in a pool shared by the segment's CTAs (not for 32-head
+        // groups, whose CTAs hold a single page lane): a CTA streams its own
+        // other pages (this lane: pg0 + pl + k NP), then claims pool pages one
+        // at a time, so the CTAs of a segment finish together whatever
+        // bandwidth each one gets.  Items of the segment are the C-aligned
+        // chunks c_first, c_first + 1, ... of [slo, shi).
+        constexpr int KDF = NH <= 2 ? kDynFrac : 0;
+        const int Cg = plan_chunk(L, a, ps, nbg, glo, ghi);
+        const unsigned long long Rg = a.plan_mode == 0 ? ps.R : recip_ceil(Cg);
+        const int c_first = div_r(slo, Rg), n_seg = div_r(shi - 1, Rg) - c_first + 1;
+        auto chunk_pages = [&](int j, int &p0, int &p1) {
+            const int c = c_first + j;
+            p0 = max(slo, c * Cg) >> 4;
+            p1 = (min(shi, (c + 1) * Cg) - 1) >> 4;
+        };
+        auto kept_back = [&](int n) { return (KDF > 0 && n >= kDynMinPages) ? max(2, n * KDF / 128) : 0; };
+        int fp0, fp1, lp0 = 0, lp1 = -1;
+        chunk_pages(0, fp0, fp1);
+        if (n_seg > 1) chunk_pages(n_seg - 1, lp0, lp1);
+        const int a_first = kept_back(fp1 - fp0 + 1);
+        const int a_mid = n_seg > 2 ? kept_back(Cg / 16) : 0;
+        const int a_last = n_seg > 1 ? kept_back(lp1 - lp0 + 1) : 0;
+        const int n_mid = n_seg > 2 ? (n_seg - 2) * a_mid : 0;
+        const int pool = a_first + n_mid + a_last;
+        const int k_self = div_r(ilo, Rg) - c_first;
+        const int kept_self = k_self == 0 ? a_first : (k_self == n_seg - 1 ? a_last : a_mid);
+        const bool dyn = pool > 0 && kept_self > 0;
+        int *const claim_ctr = L.seg_claim + 2 * bg + item.w;
+        // pool slot q -> page (-1 past the pool): the chunks' kept pages in order
+        auto pool_page = [&](int q) -> int {
+            if (q < 0 || q >= pool) return -1;
+            int j = 0, kept = a_first;
+            if (q >= a_first) {
+                q -= a_first;
+                if (q < n_mid) {
+                    j = 1 + q / a_mid;
+                    q -= (j - 1) * a_mid;
+                    kept = a_mid;
+                } else {
+                    j = n_seg - 1;
+                    q -= n_mid;
+                    kept = a_last;
+                }
+            }
+            int p0, p1;
+            chunk_pages(j, p0, p1);
+            return p1 - kept + 1 + q;
+        };
+        const int npg_own = npg - kept_self;
+        const int npl = pl < npg_own ? (npg_own - pl + NP - 1) / NP : 0;   // this lane's own pages
 
         // L2 prefetch of the page kPrefetchAhead pages past the copy front:
         // raises the bytes in flight beyond what the shared-memory stages hold
@@ -873,8 +929,7 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             prefetch_l2_bulk(L.k_pool + off, 4096);
             prefetch_l2_bulk(L.v_pool + off, 4096);
         };
-        auto issue = [&](int k) {
-            const int pg = pg0 + pl + k * NP;
+        auto issue_page = [&](int pg, int k) {   // page pg into the stage of lane step k
             const uint32_t st = lane_smem_u32 + (k % S) * kStageBytes;
             bool ok = true;
             const size_t off = kv_block(L, b, g, pg, ok);
@@ -894,19 +949,51 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         for (int k = S - 1; k < S - 1 + kPrefetchAhead; k++) prefetch(k);
 #pragma unroll
         for (int k = 0; k < S - 1; k++) {
-            if (k < npl) issue(k);
+            if (k < npl) issue_page(pg0 + pl + k * NP, k);
             cp_async_commit();
         }
-        for (int k = 0; k < npl; k++) {
+        // lane steps: own pages first, then claimed pool pages; a claim goes
+        // out one step before its page is issued (its result published in
+        // s_pool by the lane's first thread before the step's barrier)
+        int n_iss = min(npl, S - 1);   // pages this lane has issued
+        bool more = dyn;               // the pool may still hold pages for this lane
+        int pend = -2;                 // first thread: the slot claimed last step (-2: none)
+        for (int k = 0; k < n_iss; k++) {
             cp_async_wait<S - 2>();
+            if (gtid == 0 && pend != -2) {
+                const int pgc = pool_page(pend);
+                s_pool[pl][(n_iss - npl) & 7] = pgc;
+                if (pgc >= 0) {
+                    bool ok = true;
+                    const size_t off = kv_block(L, b, g, pgc, ok);
+                    if (ok) {
+                        prefetch_l2_bulk(L.k_pool + off, 4096);
+                        prefetch_l2_bulk(L.v_pool + off, 4096);
+                    }
+                }
+            }
             named_bar(1 + pl, GT);
-            if (k + S - 1 < npl) issue(k + S - 1);
+            if (n_iss == k + S - 1) {
+                int pgn = -1;
+                if (n_iss < npl) {
+                    pgn = pg0 + pl + n_iss * NP;
+                } else if (more) {
+                    pgn = s_pool[pl][(n_iss - npl) & 7];
+                    if (pgn < 0) more = false;
+                }
+                if (pgn >= 0) {
+                    issue_page(pgn, n_iss);
+                    n_iss++;
+                }
+            }
             cp_async_commit();
             prefetch(k + S - 1 + kPrefetchAhead);
+            pend = -2;
+            if (gtid == 0 && more && n_iss == k + S && k + S >= npl) pend = atomicAdd(claim_ctr, 1);
 
             const uint32_t Ks = lane_smem_u32 + (k % S) * kStageBytes;
             const uint32_t Vs = Ks + 4096;
-            const int pg = pg0 + pl + k * NP;
+            const int pg = k < npl ? pg0 + pl + k * NP : s_pool[pl][(k - npl) & 7];
 
             // S^T = K Q^T
             float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -937,12 +1024,12 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             }
             // s[0]: token r4 head hc0; s[1]: token r4 head hc1; s[2], s[3]: token r4+8
             float z0 = s[0] * sl2, z1 = s[1] * sl2, z2 = s[2] * sl2, z3 = s[3] * sl2;
-            if (pg * 16 < lo_max || pg * 16 + 16 > ihi) {
+            if (pg * 16 < lo_max || pg * 16 + 16 > shi) {
                 const int j0 = pg * 16 + r4, j1 = j0 + 8;
-                if (!(j0 >= lo0 && j0 < ihi)) z0 = -CUDART_INF_F;
-                if (!(j0 >= lo1 && j0 < ihi)) z1 = -CUDART_INF_F;
-                if (!(j1 >= lo0 && j1 < ihi)) z2 = -CUDART_INF_F;
-                if (!(j1 >= lo1 && j1 < ihi)) z3 = -CUDART_INF_F;
+                if (!(j0 >= lo0 && j0 < shi)) z0 = -CUDART_INF_F;
+                if (!(j0 >= lo1 && j0 < shi)) z1 = -CUDART_INF_F;
+                if (!(j1 >= lo0 && j1 < shi)) z2 = -CUDART_INF_F;
+                if (!(j1 >= lo1 && j1 < shi)) z3 = -CUDART_INF_F;
             }
             float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
 #pragma unroll
@@ -1132,6 +1219,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
     const float NEG = -CUDART_INF_F;
     pdl_launch_dependents();
     pdl_wait();   // partials come from the attention kernel
+    if (hh == 0 && threadIdx.x == 0) {   // the group's page pools start empty next step
+        L.seg_claim[2 * bg] = 0;
+        L.seg_claim[2 * bg + 1] = 0;
+    }
 
     float m_ring = NEG;
     float4 o_ring = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -64,7 +64,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Byte offsets of the scratch regions for one call.
 struct NoallocCarve {
-    size_t items, n_items, goff, glo, dec_lo, m_cur, kv_len, stats, err, part_ml, part_o, total;
+    size_t items, n_items, goff, glo, segc, dec_lo, m_cur, kv_len, stats, err, part_ml, part_o, total;
 };
 
 NoallocCarve carve(int batch, int heads, int kv_heads, int item_cap)
@@ -81,6 +81,7 @@ NoallocCarve carve(int batch, int heads, int kv_heads, int item_cap)
     c.n_items = take(4);
     c.goff = take(((size_t)batch * kv_heads + 1) * 4);
     c.glo = take((size_t)batch * kv_heads * 4);
+    c.segc = take((size_t)batch * kv_heads * 2 * 4);
     c.dec_lo = take((size_t)batch * heads * 4);
     c.m_cur = take((size_t)batch * 4);
     c.kv_len = take((size_t)batch * 4);
@@ -182,6 +183,7 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
     L.n_items = (int32_t *)(sc + c.n_items);
     L.grp_item_off = (int32_t *)(sc + c.goff);
     L.grp_lo = (int32_t *)(sc + c.glo);
+    L.seg_claim = (int32_t *)(sc + c.segc);
     L.dec_lo = (int32_t *)(sc + c.dec_lo);
     L.m_cur = (int32_t *)(sc + c.m_cur);
     L.kv_len = (int32_t *)(sc + c.kv_len);
