@@ -32,7 +32,7 @@ constexpr int kAttnWarps = MAC_ATTN_WARPS;         // warps per attention CTA
 constexpr int kAttnStages = MAC_ATTN_STAGES;       // pipeline stages per page lane
 constexpr int kPrefetchAhead = MAC_PREFETCH_AHEAD; // pages per lane prefetched into L2 past the copy front
 #ifndef MAC_SPECULATIVE_PAGES
-#define MAC_SPECULATIVE_PAGES 4
+#define MAC_SPECULATIVE_PAGES 2
 #endif
 constexpr int kSpeculativePages = MAC_SPECULATIVE_PAGES;  // pages per lane of the previous step's item warmed in L2
 constexpr int kStageBytes = 2 * kPage * kD * 2;   // one K page + one V page (bf16): 8 KB
