@@ -101,15 +101,27 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kernel_file):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def kernel_source_sha(files):
+    """First 16 hex digits of the SHA-256 of the kernel sources, concatenated."""
     import hashlib
+    h = hashlib.sha256()
+    for fn in files:
+        with open(fn, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = [os.path.join(ROOT, "kv_cache_computation_gb300", "csrc", f)
+                  for f in ("mac_kernels.cu", "mac_internal.cuh")]
+
+
+def profiled_traffic(kernel_files):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
     prof = os.path.join(ROOT, "profiles", "attention_kernel_128k.md")
     if not os.path.exists(prof):
         return None
-    with open(kernel_file, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    sha = kernel_source_sha(kernel_files)
     vals = {}
     for ln in open(prof):
         if ln.startswith("traffic_bytes_per_launch:") or ln.startswith("kernel_source_sha256_16:"):
@@ -465,7 +477,7 @@ def bench_ours(args, ws, rank, local):
     attn_s = prof["attention_ms"] * 1e-3
     peak, peak_kind = measured_peaks()
     achieved = attn_bytes / attn_s / 1e9 if attn_s > 0 else None
-    traffic = profiled_traffic(os.path.join(ROOT, "kv_cache_computation_gb300", "csrc", "mac_kernels.cu"))
+    traffic = profiled_traffic(KERNEL_SOURCES)
     launches = prof["steps"] or st_p["steps"]
 
     result = {
