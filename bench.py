@@ -101,6 +101,14 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def launches_per_step(cfg, amend_band):
+    """Kernels one decode step launches: Match (after the grid-wide ring scan
+    when rings are longer than 32 entries or groups have 32 heads), split-KV
+    attention, Combine, and the side-stream Amend when it recomputes the band."""
+    wide = cfg.ring_len > 32 or cfg.group == 32
+    return 3 + (1 if wide else 0) + (1 if amend_band else 0)
+
+
 def kernel_source_sha(files):
     """First 16 hex digits of the SHA-256 of the kernel sources, concatenated."""
     import hashlib
@@ -513,7 +521,7 @@ def bench_ours(args, ws, rank, local):
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         # per step: match_plan, attention, combine (+ the side-stream Amend when it recomputes the band)
-        "gpu_launches": int((3 + (1 if args.amend_band else 0)) * K_steps),
+        "gpu_launches": int(launches_per_step(cfg, args.amend_band) * K_steps),
         "clocks": clk,
         "stats": {"removal_direct": st["removal_direct"], "device_error": st["device_error"],
                   "work_items_per_step": round(items / max(1, steps), 1)},
@@ -628,7 +636,7 @@ def bench_stack(args, ws, rank, local):
         "roofline": {"kernel": "attention_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "avg_launch_us": round(attn_ms * 1e3 / launches, 3), "traffic": None},
-        "gpu_launches": int((3 + (1 if args.amend_band else 0)) * K_steps * cfg.layers),
+        "gpu_launches": int(launches_per_step(cfg, args.amend_band) * K_steps * cfg.layers),
         "clocks": clk,
     }
     for m in macs:
