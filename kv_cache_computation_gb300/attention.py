@@ -22,14 +22,16 @@ def _check(fn, status, handle=None):
         raise N.MacError(fn, status, detail)
 
 
-def _stream_ptr(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream_ptr(stream=None, device=None):
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev(t: torch.Tensor, name, dtype, shape=None):
+def _dev(t: torch.Tensor, name, dtype, shape=None, device=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the handle lives on {device}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -58,7 +60,9 @@ class MacAttention:
 
     mac_create(heads, kv_heads, head_dim, ring_len, band r, tau) plus the
     capacity (max_batch requests of up to max_ctx tokens) and the KV layout
-    (page_size 16 = paged, 0 = contiguous).
+    (page_size 16 = paged, 0 = contiguous).  Tensors passed in must live on
+    the handle's GPU, and calls are made with that GPU current (as in a
+    one-process-per-GPU program).
     """
 
     def __init__(self, heads, kv_heads, head_dim=128, ring_len=16, band_r=64, tau=0.3, max_batch=1,
@@ -96,16 +100,18 @@ class MacAttention:
 
     # -- KV -----------------------------------------------------------------
     def set_page_table(self, req: int, pages: torch.Tensor, stream=None):
-        p = _dev(pages, "pages", torch.int32)
+        p = _dev(pages, "pages", torch.int32, device=self.device)
         _check("mac_set_page_table",
-               N.lib().mac_set_page_table(self._h, req, p, pages.numel(), _stream_ptr(stream)), self._h)
+               N.lib().mac_set_page_table(self._h, req, p, pages.numel(), _stream_ptr(stream, self.device)),
+               self._h)
 
     def append_kv(self, req: int, k: torch.Tensor, v: torch.Tensor, stream=None):
         n = k.shape[0]
         shape = (n, self.kv_heads, self.head_dim)
         _check("mac_append_kv",
-               N.lib().mac_append_kv(self._h, req, _dev(k, "k", torch.bfloat16, shape),
-                                     _dev(v, "v", torch.bfloat16, shape), n, _stream_ptr(stream)), self._h)
+               N.lib().mac_append_kv(self._h, req, _dev(k, "k", torch.bfloat16, shape, device=self.device),
+                                     _dev(v, "v", torch.bfloat16, shape, device=self.device), n,
+                                     _stream_ptr(stream, self.device)), self._h)
 
     def seed_ring(self, req: int, q_pre: torch.Tensor, o: torch.Tensor, lse: torch.Tensor, positions, stream=None):
         """Insert ring entries <q~, AS_{1:pos-r}> (e.g. from the prefill) for request req."""
@@ -114,13 +120,16 @@ class MacAttention:
         if pos.shape != (n,):
             raise ValueError("one position per entry")
         _check("mac_seed_ring",
-               N.lib().mac_seed_ring(self._h, req, n, _dev(q_pre, "q_pre", torch.bfloat16, (n, self.heads, self.head_dim)),
-                                     _dev(o, "o", torch.float32, (n, self.heads, self.head_dim)),
-                                     _dev(lse, "lse", torch.float32, (n, self.heads)),
-                                     pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _stream_ptr(stream)), self._h)
+               N.lib().mac_seed_ring(self._h, req, n,
+                                     _dev(q_pre, "q_pre", torch.bfloat16, (n, self.heads, self.head_dim),
+                                          device=self.device),
+                                     _dev(o, "o", torch.float32, (n, self.heads, self.head_dim), device=self.device),
+                                     _dev(lse, "lse", torch.float32, (n, self.heads), device=self.device),
+                                     pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                     _stream_ptr(stream, self.device)), self._h)
 
     def reset_request(self, req: int, stream=None):
-        _check("mac_reset_request", N.lib().mac_reset_request(self._h, req, _stream_ptr(stream)), self._h)
+        _check("mac_reset_request", N.lib().mac_reset_request(self._h, req, _stream_ptr(stream, self.device)), self._h)
 
     # -- steps --------------------------------------------------------------
     def _outs(self, B, device, out, lse, want_lse):
@@ -128,7 +137,8 @@ class MacAttention:
             out = torch.empty((B, self.heads, self.head_dim), dtype=torch.bfloat16, device=device)
         if lse is None and want_lse:
             lse = torch.empty((B, self.heads), dtype=torch.float32, device=device)
-        lp = _dev(lse, "lse", torch.float32, (B, self.heads)) if lse is not None else ctypes.c_void_p(None)
+        lp = (_dev(lse, "lse", torch.float32, (B, self.heads), device=self.device) if lse is not None
+              else ctypes.c_void_p(None))
         return out, lse, lp
 
     def decode_step(self, q_pre, q_post, k_new, v_new, out=None, lse=None, want_lse=True, stream=None):
@@ -137,10 +147,12 @@ class MacAttention:
         B = q_pre.shape[0]
         qs, ks = (B, self.heads, self.head_dim), (B, self.kv_heads, self.head_dim)
         out, lse, lp = self._outs(B, q_pre.device, out, lse, want_lse)
-        st = N.lib().mac_decode_step(self._h, B, _dev(q_pre, "q_pre", torch.bfloat16, qs),
-                                     _dev(q_post, "q_post", torch.bfloat16, qs),
-                                     _dev(k_new, "k_new", torch.bfloat16, ks), _dev(v_new, "v_new", torch.bfloat16, ks),
-                                     _dev(out, "out", torch.bfloat16, qs), lp, _stream_ptr(stream))
+        st = N.lib().mac_decode_step(self._h, B, _dev(q_pre, "q_pre", torch.bfloat16, qs, device=self.device),
+                                     _dev(q_post, "q_post", torch.bfloat16, qs, device=self.device),
+                                     _dev(k_new, "k_new", torch.bfloat16, ks, device=self.device),
+                                     _dev(v_new, "v_new", torch.bfloat16, ks, device=self.device),
+                                     _dev(out, "out", torch.bfloat16, qs, device=self.device), lp,
+                                     _stream_ptr(stream, self.device))
         _check("mac_decode_step", st, self._h)
         return out, lse
 
@@ -149,14 +161,16 @@ class MacAttention:
         B = q_post.shape[0]
         qs, ks = (B, self.heads, self.head_dim), (B, self.kv_heads, self.head_dim)
         out, lse, lp = self._outs(B, q_post.device, out, lse, want_lse)
-        st = N.lib().mac_full_step(self._h, B, _dev(q_post, "q_post", torch.bfloat16, qs),
-                                   _dev(k_new, "k_new", torch.bfloat16, ks), _dev(v_new, "v_new", torch.bfloat16, ks),
-                                   _dev(out, "out", torch.bfloat16, qs), lp, _stream_ptr(stream))
+        st = N.lib().mac_full_step(self._h, B, _dev(q_post, "q_post", torch.bfloat16, qs, device=self.device),
+                                   _dev(k_new, "k_new", torch.bfloat16, ks, device=self.device),
+                                   _dev(v_new, "v_new", torch.bfloat16, ks, device=self.device),
+                                   _dev(out, "out", torch.bfloat16, qs, device=self.device), lp,
+                                   _stream_ptr(stream, self.device))
         _check("mac_full_step", st, self._h)
         return out, lse
 
     def join(self, stream=None):
-        _check("mac_join", N.lib().mac_join(self._h, _stream_ptr(stream)), self._h)
+        _check("mac_join", N.lib().mac_join(self._h, _stream_ptr(stream, self.device)), self._h)
 
     def sync(self, timeout_ms: int = 10000):
         _check("mac_sync", N.lib().mac_sync(self._h, timeout_ms), self._h)
@@ -182,8 +196,9 @@ class MacAttention:
     def force_decisions(self, slots: torch.Tensor, stream=None):
         B = slots.shape[0]
         _check("mac_debug_force_decisions",
-               N.lib().mac_debug_force_decisions(self._h, _dev(slots, "slots", torch.int32, (B, self.heads)), B,
-                                                 _stream_ptr(stream)), self._h)
+               N.lib().mac_debug_force_decisions(self._h, _dev(slots, "slots", torch.int32, (B, self.heads),
+                                                                 device=self.device), B,
+                                                 _stream_ptr(stream, self.device)), self._h)
 
     def decisions(self, batch: int) -> dict:
         n = batch * self.heads
