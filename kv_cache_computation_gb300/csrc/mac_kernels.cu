@@ -156,22 +156,34 @@ __device__ __forceinline__ int n_chunks(int a, int b, int C)
     return b > a ? (b - 1) / C - a / C + 1 : 0;
 }
 
-// Division by a chunk size C shared by many dividends: R = ceil(2^64 / C)
-// once, then floor(x / C) is the high word of x R.  For 0 <= x < 2^31 and
-// 2 <= C < 2^33, x R / 2^64 exceeds x / C by less than 2^-33 while the
-// fractional part of x / C is at most 1 - 1/C, so the floor is exact
-// (division by invariant integers using multiplication, Granlund and
-// Montgomery 1994).
-__device__ __forceinline__ unsigned long long recip_ceil(int C) { return ~0ull / (unsigned long long)C + 1ull; }
+// Division by a chunk size C = 16 c (4 <= c <= 2^26) shared by many
+// dividends 0 <= x < 2^30, as one 32 x 32 -> 64-bit multiply: with
+// l = ceil(log2 c), k = 26 + l and m = ceil(2^k / c) (below 2^28),
+// floor((x >> 4) m / 2^k) = floor((x >> 4) / c) = floor(x / C), because
+// (x >> 4) < 2^26 keeps the excess of the rounded-up m below 2^-l <= 1/c while
+// the fractional part of (x >> 4) / c is at most 1 - 1/c (division by
+// invariant integers using multiplication, Granlund and Montgomery 1994).
+struct ChunkDiv {
+    unsigned m;
+    int k;
+};
 
-__device__ __forceinline__ int div_r(int x, unsigned long long R)
+__device__ __forceinline__ ChunkDiv chunk_div(int C)
 {
-    return (int)__umul64hi((unsigned long long)(unsigned)x, R);
+    const unsigned c = (unsigned)C >> 4;
+    const int k = 26 + (32 - __clz(c - 1));
+    return {(unsigned)(((1ull << k) + c - 1) / c), k};
 }
 
-__device__ __forceinline__ int n_chunks_r(int a, int b, unsigned long long R)
+__device__ __forceinline__ int div_c(int x, ChunkDiv d)
 {
-    return b > a ? div_r(b - 1, R) - div_r(a, R) + 1 : 0;
+    return (int)(((unsigned long long)((unsigned)x >> 4) * d.m) >> d.k);
+}
+
+// Number of C-aligned chunks [c C, (c + 1) C) that meet [a, b).
+__device__ __forceinline__ int n_chunks_c(int a, int b, ChunkDiv d)
+{
+    return b > a ? div_c(b - 1, d) - div_c(a, d) + 1 : 0;
 }
 
 // x rounded up to a multiple of 16, clamped to 2^30 (the longest request)
@@ -258,7 +270,7 @@ struct PlanShared {
     int C;
     int total;
     long long T, Tf;
-    unsigned long long R;   // recip_ceil(C) (balanced mode)
+    ChunkDiv cd;            // chunk_div(C) (balanced mode)
 };
 
 __device__ __forceinline__ int plan_split(const Layout &L, const StepArgs &a, int lo, int hi)
@@ -300,7 +312,7 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
     }
     __syncwarp();
     int C = kMinChunk;
-    unsigned long long RC = 0;
+    ChunkDiv RC = {0u, 0};
     if (a.plan_mode == 0) {
         const int P = a.grid_ctas;
         int Q = (4 * nseg <= P) ? P : P * (1 + (2 * nseg + P - 1) / P);
@@ -320,19 +332,20 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
             const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
             long long cand = c_lo + 16 * stride * lane;
             if (cand > c_hi) cand = c_hi;
-            const unsigned long long R = recip_ceil((int)cand);
+            const ChunkDiv R = chunk_div((int)cand);
             int cnt = 0;
 #pragma unroll 4
             for (int g = 0; g < nbg; g++) {
                 const int glo = ps.lo[g], ghi = ps.hi[g], gsp = plan_split(L, a, glo, ghi);
-                cnt += n_chunks_r(glo, gsp, R) + n_chunks_r(gsp, ghi, R);
+                cnt += n_chunks_c(glo, gsp, R) + n_chunks_c(gsp, ghi, R);
             }
             const unsigned fit = __ballot_sync(0xffffffffu, cnt <= Q);
             const int k = fit ? __ffs(fit) - 1 : 31;
             const long long ck = __shfl_sync(0xffffffffu, cand, k);
             if (stride == 1 || k == 0) {
                 c_hi = ck;
-                RC = __shfl_sync(0xffffffffu, R, k);
+                RC.m = __shfl_sync(0xffffffffu, R.m, k);
+                RC.k = __shfl_sync(0xffffffffu, R.k, k);
                 break;
             }
             c_hi = ck;   // refine between the previous candidate and this one
@@ -344,7 +357,7 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
     int cnt = 0;
     if (lane < nbg) {
         if (a.plan_mode == 0) {
-            cnt = n_chunks_r(lo, sp, RC) + n_chunks_r(sp, hi, RC);
+            cnt = n_chunks_c(lo, sp, RC) + n_chunks_c(sp, hi, RC);
         } else {
             const int Cg = plan_chunk(L, a, ps, nbg, lo, hi);
             cnt = n_chunks(lo, sp, Cg) + n_chunks(sp, hi, Cg);
@@ -362,7 +375,7 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
         ps.off[nbg] = total;
         ps.total = total < L.item_cap ? total : L.item_cap;
         ps.C = C;
-        ps.R = RC;
+        ps.cd = RC;
         ps.T = T;
         ps.Tf = Tf;
     }
@@ -398,13 +411,13 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
         }
         nseg = warp_sum_int(nseg);
         int C = kMinChunk;
+        ChunkDiv RC = chunk_div(kMinChunk);
         if (a.plan_mode == 0) {
-            auto count = [&](int Cc) {
-                const unsigned long long R = recip_ceil(Cc);
+            auto count = [&](ChunkDiv R) {
                 int c = 0;
                 for (int bg = lane; bg < nbg; bg += 32) {
                     const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
-                    c += n_chunks_r(lo, sp, R) + n_chunks_r(sp, hi, R);
+                    c += n_chunks_c(lo, sp, R) + n_chunks_c(sp, hi, R);
                 }
                 return warp_sum_int(c);
             };
@@ -416,17 +429,38 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
             long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg)) : (1ll << 30);
             if (c_lo < kMinChunk) c_lo = kMinChunk;
             if (c_hi < c_lo) c_hi = c_lo;
-            while (c_lo < c_hi) {
-                long long mid = (c_lo + c_hi) / 2 / 16 * 16;
-                if (mid < c_lo) mid = c_lo;
-                if (count((int)mid) <= Q) c_hi = mid;
-                else c_lo = mid + 16;
+            // 32 candidates c_lo + 16 stride k (the last one c_hi, which fits):
+            // lane k forms candidate k's reciprocal (one division for all),
+            // a binary search over k counts the groups once per probe, and
+            // a second round refines between neighbours when stride > 1.
+            for (;;) {
+                const long long span16 = (c_hi - c_lo) / 16;
+                const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
+                long long cand = c_lo + 16 * stride * lane;
+                if (cand > c_hi) cand = c_hi;
+                const ChunkDiv R = chunk_div((int)cand);
+                int k0 = 0, k1 = (int)min(31ll, (span16 + stride - 1) / stride);   // the last distinct candidate
+                while (k0 < k1) {
+                    const int km = (k0 + k1) >> 1;
+                    const ChunkDiv Rm = {__shfl_sync(0xffffffffu, R.m, km), __shfl_sync(0xffffffffu, R.k, km)};
+                    if (count(Rm) <= Q) k1 = km;
+                    else k0 = km + 1;
+                }
+                const long long ck = __shfl_sync(0xffffffffu, cand, k0);
+                const long long cprev = __shfl_sync(0xffffffffu, cand, k0 > 0 ? k0 - 1 : 0);
+                const ChunkDiv Rk = {__shfl_sync(0xffffffffu, R.m, k0), __shfl_sync(0xffffffffu, R.k, k0)};
+                c_hi = ck;
+                if (stride == 1 || k0 == 0) {
+                    RC = Rk;
+                    break;
+                }
+                c_lo = cprev + 16;
             }
             C = (int)c_hi;
         }
         if (lane == 0) {
             ps.C = C;
-            ps.R = recip_ceil(C);
+            ps.cd = RC;
             ps.T = T;
             ps.Tf = Tf;
         }
@@ -440,7 +474,7 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
         if (bg < nbg) {
             const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
             if (a.plan_mode == 0) {
-                cnt = n_chunks_r(lo, sp, ps.R) + n_chunks_r(sp, hi, ps.R);
+                cnt = n_chunks_c(lo, sp, ps.cd) + n_chunks_c(sp, hi, ps.cd);
             } else {
                 const int C = plan_chunk(L, a, ps, nbg, lo, hi);
                 cnt = n_chunks(lo, sp, C) + n_chunks(sp, hi, C);
@@ -470,13 +504,13 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
     const int bg = g0, k = it - ps.off[bg];
     const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
     const int C = plan_chunk(L, a, ps, nbg, lo, hi);
-    const unsigned long long R = a.plan_mode == 0 ? ps.R : recip_ceil(C);
-    const int nA = n_chunks_r(lo, sp, R);
+    const ChunkDiv R = a.plan_mode == 0 ? ps.cd : chunk_div(C);
+    const int nA = n_chunks_c(lo, sp, R);
     if (k < nA) {
-        const int c = div_r(lo, R) + k;
+        const int c = div_c(lo, R) + k;
         return make_int4(bg, max(lo, c * C), min(sp, (c + 1) * C), 0);
     }
-    const int c = div_r(sp, R) + (k - nA);
+    const int c = div_c(sp, R) + (k - nA);
     return make_int4(bg, max(sp, c * C), min(hi, (c + 1) * C), 1);
 }
 
@@ -875,8 +909,8 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         // chunks c_first, c_first + 1, ... of [slo, shi).
         constexpr int KDF = NH <= 2 ? kDynFrac : 0;
         const int Cg = plan_chunk(L, a, ps, nbg, glo, ghi);
-        const unsigned long long Rg = a.plan_mode == 0 ? ps.R : recip_ceil(Cg);
-        const int c_first = div_r(slo, Rg), n_seg = div_r(shi - 1, Rg) - c_first + 1;
+        const ChunkDiv Rg = a.plan_mode == 0 ? ps.cd : chunk_div(Cg);
+        const int c_first = div_c(slo, Rg), n_seg = div_c(shi - 1, Rg) - c_first + 1;
         auto chunk_pages = [&](int j, int &p0, int &p1) {
             const int c = c_first + j;
             p0 = max(slo, c * Cg) >> 4;
@@ -891,7 +925,7 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         const int a_last = n_seg > 1 ? kept_back(lp1 - lp0 + 1) : 0;
         const int n_mid = n_seg > 2 ? (n_seg - 2) * a_mid : 0;
         const int pool = a_first + n_mid + a_last;
-        const int k_self = div_r(ilo, Rg) - c_first;
+        const int k_self = div_c(ilo, Rg) - c_first;
         const int kept_self = k_self == 0 ? a_first : (k_self == n_seg - 1 ? a_last : a_mid);
         const bool dyn = pool > 0 && kept_self > 0;
         int *const claim_ctr = L.seg_claim + 2 * bg + item.w;
