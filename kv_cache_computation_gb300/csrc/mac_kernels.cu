@@ -1189,7 +1189,7 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 }
 
 // ---------------------------------------------------------------------------
-// combine: one block of kCombineWarps warps per (request, head).  Merges the
+// combine: one block of NW warps per (request, head).  Merges the
 // group's item partials -- segment 0 (before the amend band) and segment 1
 // (the band) -- and, on a hit, the ring's AS_{1:p-r} (Figure 2(b),
 // "log-domain merge").  Items are spread over the warps so every load is in
@@ -1237,14 +1237,16 @@ __device__ __forceinline__ bool remove_band(float lf, float4 of, float lb, float
 
 // KB partials per warp per round of loads: 4, or 16 when a group may hold
 // hundreds of items (one request's single KV group spread over the grid).
+// NW warps per block: kCombineWarps, or 2 when every head has a handful of
+// items (many requests, where the grid is thousands of blocks).
 constexpr int kCombineWarps = 8;
 
-template <int KB>
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, StepArgs a)
+template <int KB, int NW>
+__global__ void __launch_bounds__(NW * 32) combine_kernel(Layout L, StepArgs a)
 {
-    __shared__ float s_red[2][kCombineWarps];
-    __shared__ float s_l[2][kCombineWarps];
-    __shared__ float4 s_o[2][kCombineWarps][32];
+    __shared__ float s_red[2][NW];
+    __shared__ float s_l[2][NW];
+    __shared__ float4 s_o[2][NW][32];
     const int gw = blockIdx.x;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = gw / L.H, h = gw - b * L.H;
@@ -1272,7 +1274,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
         }
     }
     const int off0 = L.grp_item_off[bg], off1 = L.grp_item_off[bg + 1];
-    // One pass: each warp merges items w, w + kCombineWarps, ... (segment 0
+    // One pass: each warp merges items w, w + NW, ... (segment 0
     // and segment 1 separately) online, rescaling its sums when a batch
     // raises a maximum; a shared-memory step then merges the warps.
     float mp = NEG, mb = NEG, lp = 0.f, lb = 0.f;
@@ -1283,17 +1285,17 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
         op = o_ring;
     }
     constexpr int kBatch = KB;
-    for (int i0 = off0 + w; i0 < off1; i0 += kBatch * kCombineWarps) {
+    for (int i0 = off0 + w; i0 < off1; i0 += kBatch * NW) {
         float2 ml[kBatch];
         int sg[kBatch];
         float4 ov[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; k++) {
-            const int i = min(i0 + k * kCombineWarps, off1 - 1);
+            const int i = min(i0 + k * NW, off1 - 1);
             ml[k] = L.part_ml[(size_t)i * L.G + hh];
             sg[k] = L.items[i].w;
             ov[k] = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
-            if (i0 + k * kCombineWarps >= off1) ml[k].x = NEG;   // padding slot
+            if (i0 + k * NW >= off1) ml[k].x = NEG;   // padding slot
         }
         float np = mp, nb = mb;
 #pragma unroll
@@ -1339,14 +1341,14 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(Layout L, S
     if (w != 0) return;
     float bp = NEG, bb = NEG;
 #pragma unroll
-    for (int i = 0; i < kCombineWarps; i++) {
+    for (int i = 0; i < NW; i++) {
         bp = fmaxf(bp, s_red[0][i]);
         bb = fmaxf(bb, s_red[1][i]);
     }
     lp = lb = 0.f;
     op = ob = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kCombineWarps; i++) {
+    for (int i = 0; i < NW; i++) {
         if (s_red[0][i] != NEG) {
             const float r = exp2f(s_red[0][i] - bp);
             lp = fmaf(s_l[0][i], r, lp);
@@ -1655,9 +1657,13 @@ cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
     // a group holds at most about grid / groups + 2 items
     const int nbg = a.batch * L.Hkv;
     const int per_group = (a.grid_ctas + nbg - 1) / nbg + 2;
-    const dim3 grid(a.batch * L.H), block(kCombineWarps * 32);
-    if (per_group > 128) return launch_maybe_pdl(combine_kernel<16>, grid, block, 0, s, a.pdl != 0, L, a);
-    return launch_maybe_pdl(combine_kernel<4>, grid, block, 0, s, a.pdl != 0, L, a);
+    const dim3 grid(a.batch * L.H);
+    // A few items per head (many requests): small blocks, so that the whole
+    // grid is resident beside the attention CTAs when their wait releases.
+    if (per_group <= 8) return launch_maybe_pdl(combine_kernel<4, 2>, grid, dim3(64), 0, s, a.pdl != 0, L, a);
+    const dim3 block(kCombineWarps * 32);
+    if (per_group > 128) return launch_maybe_pdl(combine_kernel<16, kCombineWarps>, grid, block, 0, s, a.pdl != 0, L, a);
+    return launch_maybe_pdl(combine_kernel<4, kCombineWarps>, grid, block, 0, s, a.pdl != 0, L, a);
 }
 
 static size_t amend_smem(int G) { return (size_t)2 * kBandTile * kBandRow + (size_t)G * kD * 2; }
