@@ -1262,14 +1262,18 @@ __global__ void __launch_bounds__(NW * 32) combine_kernel(Layout L, StepArgs a)
 
     float m_ring = NEG;
     float4 o_ring = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!a.full_mode) {
+    int m = 0, slot = 0;
+    if (!a.full_mode && w == 0) {
+        m = L.m_cur[b];   // for the epilogue, loaded alongside the rest
+        slot = L.slot_cur[b];
         const int eff = L.dec_slot[gw];
-        if (eff >= 0) {
+        if (eff >= 0) {   // summary and weight in one round trip
             const size_t e = (size_t)gw * L.ring_len + eff;
             const float lse = L.ring_lse[e];
+            const float4 o = *reinterpret_cast<const float4 *>(L.ring_o + e * kD + 4 * lane);
             if (lse != NEG) {
                 m_ring = lse * kLog2e;
-                o_ring = *reinterpret_cast<const float4 *>(L.ring_o + e * kD + 4 * lane);
+                o_ring = o;
             }
         }
     }
@@ -1389,7 +1393,6 @@ __global__ void __launch_bounds__(NW * 32) combine_kernel(Layout L, StepArgs a)
         return;
     }
     // Amend in the epilogue: the band segment is AS_{m-r+1:m}(q_m)
-    const int m = L.m_cur[b], slot = L.slot_cur[b];
     float le = NEG;
     float4 oe = make_float4(0.f, 0.f, 0.f, 0.f);
     if (m > L.band_r) {
