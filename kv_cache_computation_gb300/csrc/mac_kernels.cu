@@ -573,6 +573,23 @@ __global__ void __launch_bounds__(kScanBlock) ring_scan_kernel(Layout L, StepArg
     if (threadIdx.x == 0 && s_best != ~0ull) atomicMin(&L.dec_key[bh], s_best);
 }
 
+// One step of a transposing reduction over the 16 lanes of each half-warp:
+// N per-lane values become N / 2, lane bit N / 2 choosing which half a lane
+// keeps while it adds its partner's copy of that half.  After the steps for
+// N = 16, 8, 4, 2, v[0] of lane l is the half-warp sum of value l & 15.
+template <int N>
+__device__ __forceinline__ void halve_sum(float (&v)[16], int lane)
+{
+    constexpr int O = N / 2;
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int k = 0; k < O; k++) {
+        const float send = up ? v[k] : v[k + O];
+        const float keep = up ? v[k + O] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+    }
+}
+
 template <int MAX_THREADS, bool WIDE>
 __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepArgs a)
 {
@@ -588,19 +605,45 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
     const int m = kvlen + 1;            // 1-based position of the new token (index kvlen)
     const int slot_new = a.full_mode ? 0 : L.step_ctr[b] % L.ring_len;
 
+    // KV append of the new token: warp 0 moves K (lanes 0-15) and V (16-31).
+    // Its loads go out first; the store follows once the Match loads are
+    // in flight as well.
+    uint4 kv_val = make_uint4(0u, 0u, 0u, 0u);
+    size_t kv_off = 0;
+    bool kv_ok = true;
+    if (w == 0) {
+        kv_val = reinterpret_cast<const uint4 *>((lane < 16 ? a.k_new : a.v_new) + ((size_t)b * L.Hkv + g) * kD)[lane & 15];
+        kv_off = kv_block(L, b, g, kvlen >> 4, kv_ok);
+    }
+    auto append_new = [&]() {
+        if (w != 0) return;
+        if (kv_ok) {
+            __nv_bfloat16 *dst = (lane < 16 ? L.k_pool : L.v_pool) + kv_off + (size_t)(kvlen & 15) * kD;
+            reinterpret_cast<uint4 *>(dst)[lane & 15] = kv_val;
+        } else if (lane == 0) {
+            atomicOr(L.err, kErrPage);
+        }
+    };
+
     int lo_h = 0;
     if (!a.full_mode) {
         const int32_t *rpos = L.ring_pos + (size_t)b * L.ring_len;
         const __nv_bfloat16 *rq = L.ring_q + bh * L.ring_len * kD;
-        // Every load that depends on nothing is issued first: entry `lane`
-        // of the ring (position and query) and this head's queries.
+        // Every load that depends on nothing is issued first.  The ring's
+        // queries are read coalesced: load i of lane l is 16-byte chunk
+        // 32 i + l of the head's [L][128] block, i.e. column l & 15 of
+        // entry 2 i + (l >> 4), so each lane needs column l & 15 of q~_m
+        // alone.  A transposing reduction over each half-warp then leaves
+        // lane l the distance of entry e_own.
+        const int e_own = 2 * (lane & 15) + (lane >> 4);
         int pe0 = 0;
         uint4 c[16];
-        if (!WIDE && lane < L.ring_len) {
-            pe0 = rpos[lane];
-            const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)lane * kD);
+        if (!WIDE) {
+            const int nch = L.ring_len * kD / 8;
+            const uint4 *blk = reinterpret_cast<const uint4 *>(rq);
 #pragma unroll
-            for (int i = 0; i < 16; i++) c[i] = ent[i];
+            for (int i = 0; i < 16; i++) c[i] = 32 * i + lane < nch ? blk[32 * i + lane] : make_uint4(0u, 0u, 0u, 0u);
+            if (e_own < L.ring_len) pe0 = rpos[e_own];
         }
         if (lane < 16) {
             s_q[w][lane] = reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[lane];
@@ -608,27 +651,10 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
             reinterpret_cast<uint4 *>(L.q_stash + bh * kD)[lane - 16] =
                 reinterpret_cast<const uint4 *>(a.q_post + bh * kD)[lane - 16];
         }
+        append_new();
         __syncwarp();
         const float4 q4 = load_bf16x4(reinterpret_cast<const __nv_bfloat16 *>(s_q[w]) + 4 * lane);
         const float qn2 = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
-        // D_e = ||q~_m - q~_e||^2 in fp32 for the entries this lane owns
-        auto dist = [&](const uint4 (&cc)[16]) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const uint4 qq = s_q[w][i];
-                const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w}, ca[4] = {cc[i].x, cc[i].y, cc[i].z, cc[i].w};
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[j]));
-                    const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ca[j]));
-                    const float d0 = qf.x - cf.x, d1 = qf.y - cf.y;
-                    acc[j] = fmaf(d0, d0, acc[j]);
-                    acc[j] = fmaf(d1, d1, acc[j]);
-                }
-            }
-            return (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        };
         int best = -1, best_pos = 0;
         float bestD = CUDART_INF_F;
         if (WIDE) {   // the scan kernel left the best (distance, age) key
@@ -641,22 +667,34 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
             }
             __syncwarp();
             if (lane == 0) L.dec_key[bh] = ~0ull;   // ready for the next step
-        } else if (pe0 > 0) {
-            best = lane;
-            bestD = dist(c);
-            best_pos = pe0;
-        }
-        for (int e = lane + 32; !WIDE && e < L.ring_len; e += 32) {   // rings longer than a warp
-            const int pe = rpos[e];
-            if (pe <= 0) continue;
-            const uint4 *ent = reinterpret_cast<const uint4 *>(rq + (size_t)e * kD);
+        } else {
+            // D_e = ||q~_m - q~_e||^2 in fp32: this lane's column of every
+            // chunk it loaded, then the half-warp sums
+            const uint4 qq = s_q[w][lane & 15];
+            const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w};
+            float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; i++) c[i] = ent[i];
-            const float De = dist(c);
-            if (best < 0 || De < bestD || (De == bestD && pe > best_pos)) {
-                best = e;
-                bestD = De;
-                best_pos = pe;
+            for (int i = 0; i < 16; i++) {
+                const uint32_t ca[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[j]));
+                    const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ca[j]));
+                    const float d0 = qf.x - cf.x, d1 = qf.y - cf.y;
+                    acc = fmaf(d0, d0, acc);
+                    acc = fmaf(d1, d1, acc);
+                }
+                v[i] = acc;
+            }
+            halve_sum<16>(v, lane);
+            halve_sum<8>(v, lane);
+            halve_sum<4>(v, lane);
+            halve_sum<2>(v, lane);
+            if (pe0 > 0) {
+                best = e_own;
+                bestD = v[0];
+                best_pos = pe0;
             }
         }
 #pragma unroll
@@ -703,18 +741,7 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
         L.dec_lo[bh] = 0;
     }
 
-    // KV append of the new token: warp 0 moves K (lanes 0-15) and V (16-31).
-    if (w == 0) {
-        bool ok = true;
-        const size_t off = kv_block(L, b, g, kvlen >> 4, ok);
-        if (ok) {
-            const __nv_bfloat16 *src = (lane < 16 ? a.k_new : a.v_new) + ((size_t)b * L.Hkv + g) * kD;
-            __nv_bfloat16 *dst = (lane < 16 ? L.k_pool : L.v_pool) + off + (size_t)(kvlen & 15) * kD;
-            reinterpret_cast<uint4 *>(dst)[lane & 15] = reinterpret_cast<const uint4 *>(src)[lane & 15];
-        } else if (lane == 0) {
-            atomicOr(L.err, kErrPage);
-        }
-    }
+    if (a.full_mode) append_new();
     if (g == 0 && threadIdx.x == 0) {
         L.m_cur[b] = m;
         L.slot_cur[b] = slot_new;
