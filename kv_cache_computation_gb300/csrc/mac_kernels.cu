@@ -517,12 +517,15 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
 // ---------------------------------------------------------------------------
 // match_plan: grid (Hkv, batch), block G warps (warp w = query head g*G + w).
 // Leaves per group the span start lo_g; the attention kernel plans from it.
-// Match (Figure 2(a)): lane e evaluates ring entry e (and e+32), so all the
-// ring's loads are in flight at once; a warp argmin then picks the nearest
-// entry (ties to the larger position).
+// Match (Figure 2(a)): one warp per query head reads the head's ring
+// queries coalesced, all loads in flight at once, and ends with one entry's
+// distance per lane; a warp argmin then picks the nearest entry (ties to the
+// larger position).
 // ---------------------------------------------------------------------------
 // ---------------------------------------------------------------------------
-// Wide rings (more than kSmallRing entries): every entry is one thread of a
+// Wide rings (more than kSmallRing entries, or more than 16 in a 32-head
+// group, whose 1024-thread Match block has registers for 16 entries' loads
+// per lane): every entry is one thread of a
 // (split, head, request) block; the block's best (distance, age) key goes
 // into dec_key with a 64-bit atomic minimum.  Distances are non-negative, so
 // their float bits order as unsigned integers; age 0 is the newest entry,
@@ -590,7 +593,9 @@ __device__ __forceinline__ void halve_sum(float (&v)[16], int lane)
     }
 }
 
-template <int MAX_THREADS, bool WIDE>
+// NI: 16-byte loads per lane for the ring's queries, 8 for rings of up to
+// 16 entries, 16 for up to 32 (unused by the wide form).
+template <int MAX_THREADS, bool WIDE, int NI>
 __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepArgs a)
 {
     __shared__ __align__(16) uint4 s_q[32][16];
@@ -637,12 +642,12 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
         // lane l the distance of entry e_own.
         const int e_own = 2 * (lane & 15) + (lane >> 4);
         int pe0 = 0;
-        uint4 c[16];
+        uint4 c[NI];
         if (!WIDE) {
             const int nch = L.ring_len * kD / 8;
             const uint4 *blk = reinterpret_cast<const uint4 *>(rq);
 #pragma unroll
-            for (int i = 0; i < 16; i++) c[i] = 32 * i + lane < nch ? blk[32 * i + lane] : make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < NI; i++) c[i] = 32 * i + lane < nch ? blk[32 * i + lane] : make_uint4(0u, 0u, 0u, 0u);
             if (e_own < L.ring_len) pe0 = rpos[e_own];
         }
         if (lane < 16) {
@@ -674,7 +679,9 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
             const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w};
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
+            for (int i = NI; i < 16; i++) v[i] = 0.f;   // entries past 2 NI: none
+#pragma unroll
+            for (int i = 0; i < NI; i++) {
                 const uint32_t ca[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
                 float acc = 0.f;
 #pragma unroll
@@ -1650,18 +1657,21 @@ static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem
 
 cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    // up to 16 heads per group: a 512-thread bound leaves room for the ring
-    // entry held in registers during Match
+    // One warp per query head.  Up to 16 heads per group a 512-thread bound
+    // leaves room for 32 ring entries' loads in registers; 32-head groups
+    // (1024 threads) hold 16 entries' loads.  Larger rings go through the
+    // scan kernel first.
     const dim3 grid(L.Hkv, a.batch), block(L.G * 32);
-    if (L.G <= 16 && (a.full_mode || L.ring_len <= kSmallRing))
-        return launch_maybe_pdl(match_plan_kernel<512, false>, grid, block, 0, s, a.pdl, L, a);
-    if (a.full_mode)   // no ring work: the wide instantiation only appends and plans
-        return launch_maybe_pdl(match_plan_kernel<1024, true>, grid, block, 0, s, a.pdl, L, a);
+    const bool small = a.full_mode || L.ring_len <= 16;
+    if (L.G <= 16 && small) return launch_maybe_pdl(match_plan_kernel<512, false, 8>, grid, block, 0, s, a.pdl, L, a);
+    if (L.G <= 16 && L.ring_len <= kSmallRing)
+        return launch_maybe_pdl(match_plan_kernel<512, false, 16>, grid, block, 0, s, a.pdl, L, a);
+    if (small) return launch_maybe_pdl(match_plan_kernel<1024, false, 8>, grid, block, 0, s, a.pdl, L, a);
     const dim3 sgrid((L.ring_len + kScanBlock - 1) / kScanBlock, L.H, a.batch);
     cudaError_t e = launch_maybe_pdl(ring_scan_kernel, sgrid, dim3(kScanBlock), 0, s, a.pdl, L, a);
     if (e != cudaSuccess) return e;
-    if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512, true>, grid, block, 0, s, a.pdl, L, a);
-    return launch_maybe_pdl(match_plan_kernel<1024, true>, grid, block, 0, s, a.pdl, L, a);
+    if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512, true, 8>, grid, block, 0, s, a.pdl, L, a);
+    return launch_maybe_pdl(match_plan_kernel<1024, true, 8>, grid, block, 0, s, a.pdl, L, a);
 }
 
 cudaError_t launch_seed(const Layout &L, int req, int first, int n, int base_step, const __nv_bfloat16 *q,
