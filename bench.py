@@ -103,10 +103,9 @@ def measured_peaks():
 
 def launches_per_step(cfg, amend_band):
     """Kernels one decode step launches: Match (after the grid-wide ring scan
-    when rings are longer than 32 entries, or than 16 in 32-head groups),
-    split-KV attention, Combine, and the side-stream Amend when it recomputes
-    the band."""
-    wide = cfg.ring_len > 32 or (cfg.group > 16 and cfg.ring_len > 16)
+    when rings are longer than 32 entries), split-KV attention, Combine, and
+    the side-stream Amend when it recomputes the band."""
+    wide = cfg.ring_len > 32
     return 3 + (1 if wide else 0) + (1 if amend_band else 0)
 
 

@@ -73,8 +73,8 @@ typedef struct {
                         /* G = heads / kv_heads is one of 1, 2, 4, 8, 16, 32     */
     int head_dim;       /* d; must be 128                                        */
     int ring_len;       /* L: ring entries per (request, head), 1..4096; rings   */
-                        /* over 32 entries (or groups of 32 heads) are scanned  */
-                        /* by a separate grid-wide kernel before Match decides  */
+                        /* over 32 entries are scanned by a separate grid-wide  */
+                        /* kernel before Match decides                          */
     int band_r;         /* r: rectification band width in tokens, >= 1           */
     double tau;         /* L2 threshold, relative: hit iff                       */
                         /* ||q~_m - q~_e|| < tau * ||q~_m||; tau >= 0           */

@@ -421,6 +421,7 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     L.H = cfg->heads;
     L.Hkv = cfg->kv_heads;
     L.G = z.G;
+    L.lo_parts = match_parts(z.G);
     L.ring_len = cfg->ring_len;
     L.band_r = cfg->band_r;
     L.max_batch = cfg->max_batch;
@@ -480,6 +481,8 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     if (e != cudaSuccess) return fail(e, "cudaMemset(ring positions)");
     e = cudaMemset(sc + z.s_dkey, 0xff, (size_t)cfg->max_batch * cfg->heads * 8);   // "no entry" keys
     if (e != cudaSuccess) return fail(e, "cudaMemset(match keys)");
+    e = cudaMemset(sc + z.s_glo, 0x7f, (size_t)cfg->max_batch * cfg->kv_heads * 4);   // above any position
+    if (e != cudaSuccess) return fail(e, "cudaMemset(group span starts)");
     int lo_prio = 0, hi_prio = 0;
     e = cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio);
     if (e != cudaSuccess) return fail(e, "cudaDeviceGetStreamPriorityRange");

@@ -16,6 +16,11 @@ constexpr int kSmallRing = 32;          // rings up to this size (one entry per 
                                         // the Match kernel, for groups of up to 16 heads
 constexpr int kScanBlock = 256;         // ring entries per block of the wide-ring scan
 constexpr int kMaxGroup = 32;           // query heads per KV head
+constexpr int kMatchWarps = 8;          // query heads (warps) per Match block at most
+
+// Match blocks per group: groups of more than kMatchWarps heads are split
+// so that no SM holds more than kMatchWarps heads' ring scans.
+inline __host__ __device__ int match_parts(int G) { return (G + kMatchWarps - 1) / kMatchWarps; }
 constexpr int kMaxCtas = 1024;          // upper bound of the attention grid
 constexpr int kMaxGroupsPerStep = 1024; // max_batch * kv_heads (the plan is held in shared memory)
 // attention pipeline shape (overridable at build time for tuning sweeps)
@@ -115,6 +120,9 @@ struct Layout {
 
     unsigned long long *stats;        // [kStCount]
     uint32_t *err;
+
+    int lo_parts;   // Match blocks per group (match_parts(G)); above 1 they meet in grp_lo by atomicMin
+                    // and Combine sets the word back to INT_MAX for the next step
 };
 
 struct StepArgs {

@@ -515,17 +515,18 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
 }
 
 // ---------------------------------------------------------------------------
-// match_plan: grid (Hkv, batch), block G warps (warp w = query head g*G + w).
-// Leaves per group the span start lo_g; the attention kernel plans from it.
+// match_plan: grid (lo_parts, Hkv, batch); block = part `part` of group g,
+// nw = ceil(G / lo_parts) warps, warp w = query head g G + part nw + w.
+// Leaves per group the span start lo_g (the parts of a split group take
+// their minimum with atomicMin on a word Combine resets every step); the
+// attention kernel plans from it.
 // Match (Figure 2(a)): one warp per query head reads the head's ring
 // queries coalesced, all loads in flight at once, and ends with one entry's
 // distance per lane; a warp argmin then picks the nearest entry (ties to the
 // larger position).
 // ---------------------------------------------------------------------------
 // ---------------------------------------------------------------------------
-// Wide rings (more than kSmallRing entries, or more than 16 in a 32-head
-// group, whose 1024-thread Match block has registers for 16 entries' loads
-// per lane): every entry is one thread of a
+// Wide rings (more than kSmallRing entries): every entry is one thread of a
 // (split, head, request) block; the block's best (distance, age) key goes
 // into dec_key with a 64-bit atomic minimum.  Distances are non-negative, so
 // their float bits order as unsigned integers; age 0 is the newest entry,
@@ -594,17 +595,23 @@ __device__ __forceinline__ void halve_sum(float (&v)[16], int lane)
 }
 
 // NI: 16-byte loads per lane for the ring's queries, 8 for rings of up to
-// 16 entries, 16 for up to 32 (unused by the wide form).
-template <int MAX_THREADS, bool WIDE, int NI>
+// 16 entries, 16 for up to 32 (unused by the wide form).  SPLIT: the group
+// is spread over L.lo_parts blocks (groups of more than kMatchWarps heads).
+template <int MAX_THREADS, bool WIDE, int NI, bool SPLIT>
 __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepArgs a)
 {
-    __shared__ __align__(16) uint4 s_q[32][16];
+    constexpr int NWM = MAX_THREADS / 32;
+    __shared__ __align__(16) uint4 s_q[NWM][16];
     pdl_launch_dependents();
     pdl_wait();   // launched early behind the previous step: read nothing before its completion
-    const int g = blockIdx.x, b = blockIdx.y;
+    // block = part `part` of group g: its heads part * nw + w, w < nw
+    const int part = SPLIT ? blockIdx.x : 0, g = blockIdx.y, b = blockIdx.z;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = L.G, H = L.H;
-    const int h = g * G + w;
+    const int nw = blockDim.x >> 5;
+    const int gh = part * nw + w;        // head within the group
+    const bool active = !SPLIT || gh < G;
+    const int h = g * G + gh;
     const size_t bh = (size_t)b * H + h;
     const int kvlen = L.kv_len[b];
     const int m = kvlen + 1;            // 1-based position of the new token (index kvlen)
@@ -613,15 +620,16 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
     // KV append of the new token: warp 0 moves K (lanes 0-15) and V (16-31).
     // Its loads go out first; the store follows once the Match loads are
     // in flight as well.
+    const bool appender = w == 0 && part == 0;
     uint4 kv_val = make_uint4(0u, 0u, 0u, 0u);
     size_t kv_off = 0;
     bool kv_ok = true;
-    if (w == 0) {
+    if (appender) {
         kv_val = reinterpret_cast<const uint4 *>((lane < 16 ? a.k_new : a.v_new) + ((size_t)b * L.Hkv + g) * kD)[lane & 15];
         kv_off = kv_block(L, b, g, kvlen >> 4, kv_ok);
     }
     auto append_new = [&]() {
-        if (w != 0) return;
+        if (!appender) return;
         if (kv_ok) {
             __nv_bfloat16 *dst = (lane < 16 ? L.k_pool : L.v_pool) + kv_off + (size_t)(kvlen & 15) * kD;
             reinterpret_cast<uint4 *>(dst)[lane & 15] = kv_val;
@@ -630,8 +638,9 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
         }
     };
 
-    int lo_h = 0;
-    if (!a.full_mode) {
+    int lo_h = 0x7fffffff;
+    if (!active) {
+    } else if (!a.full_mode) {
         const int32_t *rpos = L.ring_pos + (size_t)b * L.ring_len;
         const __nv_bfloat16 *rq = L.ring_q + bh * L.ring_len * kD;
         // Every load that depends on nothing is issued first.  The ring's
@@ -743,25 +752,29 @@ __global__ void __launch_bounds__(MAX_THREADS) match_plan_kernel(Layout L, StepA
         // queries before that Amend has run.
         __syncwarp();
         if (lane < 16) reinterpret_cast<uint4 *>(L.ring_q + (bh * L.ring_len + slot_new) * kD)[lane] = s_q[w][lane];
-    } else if (lane == 0) {
-        L.dec_slot[bh] = -1;
-        L.dec_lo[bh] = 0;
+    } else {
+        lo_h = 0;
+        if (lane == 0) {
+            L.dec_slot[bh] = -1;
+            L.dec_lo[bh] = 0;
+        }
     }
 
     if (a.full_mode) append_new();
-    if (g == 0 && threadIdx.x == 0) {
+    if (g == 0 && part == 0 && threadIdx.x == 0) {
         L.m_cur[b] = m;
         L.slot_cur[b] = slot_new;
     }
 
-    // group span start = min over the group's heads
-    __shared__ int s_glo[32];
+    // span start of this block's heads, then of the group
+    __shared__ int s_glo[NWM];
     if (lane == 0) s_glo[w] = lo_h;
     __syncthreads();
     if (threadIdx.x == 0) {
         int lo = s_glo[0];
-        for (int i = 1; i < G; i++) lo = min(lo, s_glo[i]);
-        L.grp_lo[(size_t)b * L.Hkv + g] = lo;
+        for (int i = 1; i < nw; i++) lo = min(lo, s_glo[i]);
+        if (SPLIT) atomicMin(&L.grp_lo[(size_t)b * L.Hkv + g], lo);
+        else L.grp_lo[(size_t)b * L.Hkv + g] = lo;
     }
 }
 
@@ -1292,6 +1305,7 @@ __global__ void __launch_bounds__(NW * 32) combine_kernel(Layout L, StepArgs a)
     if (hh == 0 && threadIdx.x == 0) {   // the group's page pools start empty next step
         L.seg_claim[2 * bg] = 0;
         L.seg_claim[2 * bg + 1] = 0;
+        if (L.lo_parts > 1) L.grp_lo[bg] = 0x7fffffff;   // split Match groups meet by atomicMin
     }
 
     float m_ring = NEG;
@@ -1657,21 +1671,26 @@ static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem
 
 cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    // One warp per query head.  Up to 16 heads per group a 512-thread bound
-    // leaves room for 32 ring entries' loads in registers; 32-head groups
-    // (1024 threads) hold 16 entries' loads.  Larger rings go through the
-    // scan kernel first.
-    const dim3 grid(L.Hkv, a.batch), block(L.G * 32);
-    const bool small = a.full_mode || L.ring_len <= 16;
-    if (L.G <= 16 && small) return launch_maybe_pdl(match_plan_kernel<512, false, 8>, grid, block, 0, s, a.pdl, L, a);
-    if (L.G <= 16 && L.ring_len <= kSmallRing)
-        return launch_maybe_pdl(match_plan_kernel<512, false, 16>, grid, block, 0, s, a.pdl, L, a);
-    if (small) return launch_maybe_pdl(match_plan_kernel<1024, false, 8>, grid, block, 0, s, a.pdl, L, a);
-    const dim3 sgrid((L.ring_len + kScanBlock - 1) / kScanBlock, L.H, a.batch);
-    cudaError_t e = launch_maybe_pdl(ring_scan_kernel, sgrid, dim3(kScanBlock), 0, s, a.pdl, L, a);
-    if (e != cudaSuccess) return e;
-    if (L.G <= 16) return launch_maybe_pdl(match_plan_kernel<512, true, 8>, grid, block, 0, s, a.pdl, L, a);
-    return launch_maybe_pdl(match_plan_kernel<1024, true, 8>, grid, block, 0, s, a.pdl, L, a);
+    // One warp per query head, at most kMatchWarps heads per block (a group
+    // of more heads is split over L.lo_parts blocks).  Rings of more than
+    // kSmallRing entries go through the scan kernel first.
+    constexpr int T = kMatchWarps * 32;
+    const int nw = (L.G + L.lo_parts - 1) / L.lo_parts;
+    const dim3 grid(L.lo_parts, L.Hkv, a.batch), block(nw * 32);
+    const int form = a.full_mode || L.ring_len <= 16 ? 0 : L.ring_len <= kSmallRing ? 1 : 2;
+    if (form == 2) {
+        const dim3 sgrid((L.ring_len + kScanBlock - 1) / kScanBlock, L.H, a.batch);
+        cudaError_t e = launch_maybe_pdl(ring_scan_kernel, sgrid, dim3(kScanBlock), 0, s, a.pdl, L, a);
+        if (e != cudaSuccess) return e;
+    }
+    if (L.lo_parts == 1) {
+        if (form == 0) return launch_maybe_pdl(match_plan_kernel<512, false, 8, false>, grid, block, 0, s, a.pdl, L, a);
+        if (form == 1) return launch_maybe_pdl(match_plan_kernel<512, false, 16, false>, grid, block, 0, s, a.pdl, L, a);
+        return launch_maybe_pdl(match_plan_kernel<512, true, 8, false>, grid, block, 0, s, a.pdl, L, a);
+    }
+    if (form == 0) return launch_maybe_pdl(match_plan_kernel<T, false, 8, true>, grid, block, 0, s, a.pdl, L, a);
+    if (form == 1) return launch_maybe_pdl(match_plan_kernel<T, false, 16, true>, grid, block, 0, s, a.pdl, L, a);
+    return launch_maybe_pdl(match_plan_kernel<T, true, 8, true>, grid, block, 0, s, a.pdl, L, a);
 }
 
 cudaError_t launch_seed(const Layout &L, int req, int first, int n, int base_step, const __nv_bfloat16 *q,

@@ -169,6 +169,7 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
     L.H = heads;
     L.Hkv = kv_heads;
     L.G = G;
+    L.lo_parts = 1;   // grp_lo is written by noalloc_prepare_kernel
     L.ring_len = 1;
     L.band_r = 1;
     L.max_batch = batch;

@@ -80,13 +80,14 @@ def test_mac_chain_group_sizes(kv_heads, amend_band):
         p.mac_step(t, force=True)
 
 
-@pytest.mark.parametrize("kv_heads,ring_len", [(1, 16), (1, 17), (1, 32), (8, 16), (8, 17), (8, 32), (8, 33)])
+@pytest.mark.parametrize("kv_heads,ring_len", [(1, 16), (1, 17), (1, 32), (1, 33), (8, 16), (8, 17), (8, 32), (8, 33),
+                                               (2, 20), (4, 9)])
 def test_match_forms_at_their_ring_size_limits(kv_heads, ring_len):
-    """Each form of Match on both sides of the ring size where the dispatch
-    changes: 32-head groups scan up to 16 entries in their own block (8 loads
-    per lane) and longer rings through the scan kernel; smaller groups scan up
-    to 16 and up to 32 entries in their own block (8 or 16 loads per lane) and
-    longer rings through the scan kernel.  The ring fills and wraps."""
+    """Each form of Match on both sides of the ring sizes where it changes:
+    up to 16 and up to 32 entries scanned in the Match block (8 or 16 loads
+    per lane), longer rings through the scan kernel first.  Groups of 32
+    heads (four Match blocks of 8), 16 heads (two of 8), 8 and 4 heads (one
+    block).  The ring fills and wraps."""
     steps = ring_len + 6
     p = _pair(cfg(kv_heads=kv_heads, context=300, steps=steps, rho=0.995, ring_len=ring_len))
     hits = 0
