@@ -1191,6 +1191,30 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             l0 += __shfl_xor_sync(0xffffffffu, l0, o);
             l1 += __shfl_xor_sync(0xffffffffu, l1, o);
         }
+        if constexpr (NP == 1) {   // one page lane: the fragments are the item's partial
+            const float NEG = -CUDART_INF_F;
+            if (hc0 < G) {
+                float *o0 = L.part_o + ((size_t)it * G + hc0) * kD;
+                const bool none = m0 == NEG;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    o0[16 * i + r4] = none ? 0.f : acc[i][0];
+                    o0[16 * i + r4 + 8] = none ? 0.f : acc[i][2];
+                }
+                if (r4 == 0) L.part_ml[(size_t)it * G + hc0] = make_float2(m0, none ? 0.f : l0);
+            }
+            if (hc1 < G) {
+                float *o1 = L.part_o + ((size_t)it * G + hc1) * kD;
+                const bool none = m1 == NEG;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    o1[16 * i + r4] = none ? 0.f : acc[i][1];
+                    o1[16 * i + r4 + 8] = none ? 0.f : acc[i][3];
+                }
+                if (r4 == 0) L.part_ml[(size_t)it * G + hc1] = make_float2(m1, none ? 0.f : l1);
+            }
+            continue;   // the stage memory was drained above; nothing else is staged
+        }
         // stage each page lane's partial in shared memory, then merge lanes
         float *red_o = reinterpret_cast<float *>(smem);                               // [NP][G][D]
         float2 *red_ml = reinterpret_cast<float2 *>(red_o + (size_t)NP * G * kD);     // [NP][G]
