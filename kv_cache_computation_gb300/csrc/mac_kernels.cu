@@ -525,58 +525,6 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
 // distance per lane; a warp argmin then picks the nearest entry (ties to the
 // larger position).
 // ---------------------------------------------------------------------------
-// ---------------------------------------------------------------------------
-// Wide rings (more than kSmallRing entries): every entry is one thread of a
-// (split, head, request) block; the block's best (distance, age) key goes
-// into dec_key with a 64-bit atomic minimum.  Distances are non-negative, so
-// their float bits order as unsigned integers; age 0 is the newest entry,
-// so equal distances resolve to the most recent position.
-// grid (ceil(L / kScanBlock), H, batch), block kScanBlock threads.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kScanBlock) ring_scan_kernel(Layout L, StepArgs a)
-{
-    __shared__ __align__(16) uint4 sq[16];
-    __shared__ unsigned long long s_best;
-    pdl_launch_dependents();
-    pdl_wait();   // launched early behind the previous step: read nothing before its completion
-    const int h = blockIdx.y, b = blockIdx.z;
-    const size_t bh = (size_t)b * L.H + h;
-    if (threadIdx.x < 16) sq[threadIdx.x] = reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[threadIdx.x];
-    if (threadIdx.x == 0) s_best = ~0ull;
-    __syncthreads();
-    const int e = blockIdx.x * kScanBlock + threadIdx.x;
-    const int step = L.step_ctr[b];
-    if (e < L.ring_len) {
-        const int pe = L.ring_pos[(size_t)b * L.ring_len + e];
-        if (pe > 0) {
-            const uint4 *ent = reinterpret_cast<const uint4 *>(L.ring_q + (bh * L.ring_len + e) * kD);
-            uint4 c[16];
-#pragma unroll
-            for (int i = 0; i < 16; i++) c[i] = ent[i];
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const uint4 qq = sq[i];
-                const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w}, ca[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[j]));
-                    const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ca[j]));
-                    const float d0 = qf.x - cf.x, d1 = qf.y - cf.y;
-                    acc[j] = fmaf(d0, d0, acc[j]);
-                    acc[j] = fmaf(d1, d1, acc[j]);
-                }
-            }
-            const float De = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            const int age = ((step - 1 - e) % L.ring_len + L.ring_len) % L.ring_len;
-            const unsigned long long key = ((unsigned long long)__float_as_uint(De) << 32) | (unsigned)age;
-            atomicMin(&s_best, key);
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && s_best != ~0ull) atomicMin(&L.dec_key[bh], s_best);
-}
-
 // One step of a transposing reduction over the 16 lanes of each half-warp:
 // N per-lane values become N / 2, lane bit N / 2 choosing which half a lane
 // keeps while it adds its partner's copy of that half.  After the steps for
@@ -592,6 +540,79 @@ __device__ __forceinline__ void halve_sum(float (&v)[16], int lane)
         const float keep = up ? v[k + O] : v[k];
         v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Wide rings (more than kSmallRing entries): warp w of a (split, head,
+// request) block scans entries 32 w .. 32 w + 31 of the split with the
+// Match kernel's coalesced layout (load i of lane l = column l & 15 of
+// entries 2 i and 2 i + 1, then the transposing half-warp reduction); the
+// block's best (distance, age) key goes into dec_key with a 64-bit atomic
+// minimum.  Distances are non-negative, so their float bits order as
+// unsigned integers; age 0 is the newest entry, so equal distances resolve
+// to the most recent position.
+// grid (ceil(L / kScanBlock), H, batch), block kScanBlock threads.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScanBlock, 2) ring_scan_kernel(Layout L, StepArgs a)
+{
+    __shared__ __align__(16) uint4 sq[16];
+    __shared__ unsigned long long s_best;
+    pdl_launch_dependents();
+    pdl_wait();   // launched early behind the previous step: read nothing before its completion
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t bh = (size_t)b * L.H + h;
+    const int e0 = blockIdx.x * kScanBlock + 32 * w;      // this warp's first entry
+    const int e = e0 + 2 * (lane & 15) + (lane >> 4);     // the entry whose distance this lane ends with
+    uint4 c[16];
+    int pe = 0;
+    if (e0 < L.ring_len) {
+        const int nch = (L.ring_len - e0) * (kD / 8);      // 16-byte chunks of this warp's entries
+        const uint4 *blk = reinterpret_cast<const uint4 *>(L.ring_q + (bh * L.ring_len + e0) * kD);
+#pragma unroll
+        for (int i = 0; i < 16; i++) c[i] = 32 * i + lane < nch ? blk[32 * i + lane] : make_uint4(0u, 0u, 0u, 0u);
+        if (e < L.ring_len) pe = L.ring_pos[(size_t)b * L.ring_len + e];
+    }
+    if (threadIdx.x < 16) sq[threadIdx.x] = reinterpret_cast<const uint4 *>(a.q_pre + bh * kD)[threadIdx.x];
+    if (threadIdx.x == 0) s_best = ~0ull;
+    const int step = L.step_ctr[b];
+    __syncthreads();
+    if (e0 < L.ring_len) {
+        const uint4 qq = sq[lane & 15];
+        const uint32_t qa[4] = {qq.x, qq.y, qq.z, qq.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const uint32_t ca[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[j]));
+                const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ca[j]));
+                const float d0 = qf.x - cf.x, d1 = qf.y - cf.y;
+                acc = fmaf(d0, d0, acc);
+                acc = fmaf(d1, d1, acc);
+            }
+            v[i] = acc;
+        }
+        halve_sum<16>(v, lane);
+        halve_sum<8>(v, lane);
+        halve_sum<4>(v, lane);
+        halve_sum<2>(v, lane);
+        unsigned long long key = ~0ull;
+        if (pe > 0) {
+            const int age = ((step - 1 - e) % L.ring_len + L.ring_len) % L.ring_len;
+            key = ((unsigned long long)__float_as_uint(v[0]) << 32) | (unsigned)age;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const unsigned long long ok = __shfl_xor_sync(0xffffffffu, key, o);
+            key = ok < key ? ok : key;
+        }
+        if (lane == 0 && key != ~0ull) atomicMin(&s_best, key);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && s_best != ~0ull) atomicMin(&L.dec_key[bh], s_best);
 }
 
 // NI: 16-byte loads per lane for the ring's queries, 8 for rings of up to
