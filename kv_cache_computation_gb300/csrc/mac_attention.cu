@@ -1,0 +1,808 @@
+// sm_103a split-KV attention of the MAC-Attention decode step (Complete,
+// Figure 2(b) of the MAC-Attention paper) and the span-proportional planner
+// every CTA runs in its prologue (Figure 3(b), "load-balanced planning").
+//
+// Conventions: token index j (0-based) is the paper's position j+1; ranges
+// [lo, hi) are half-open over indices.  Scores are kept in log2 units
+// (scaled by sm_scale * log2 e) inside the kernels.
+#include "mac_device.cuh"
+
+namespace macgpu {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Planning (prologue of every attention CTA; all CTAs derive the same plan).
+// Per (request, kv-head) group the streamed span is [lo_g, m), lo_g being the
+// smallest band+tail start of the group's heads.  Amend's band [m-r, m) is
+// cut off as its own segment, so Complete yields the rectification term
+// AS_{m-r+1:m} and the direct form of AS_{1:m-r} as by-products.  Chunks are
+// cut at multiples of C (a multiple of 16: page aligned).
+//
+// Balanced mode (Figure 3(b), "load-balanced planning"): every item costs at
+// most C tokens, so the step finishes when the longest item does; the plan
+// takes the smallest C for which the items fit one wave of the persistent
+// attention grid (or k waves when there are more segments than CTAs).
+// Longer spans thereby get proportionally more CTAs.  Equal mode gives every
+// group the same number of items whatever its span (unbalanced baseline).
+// ---------------------------------------------------------------------------
+struct PlanShared {
+    int lo[kPlanCache];
+    int hi[kPlanCache];
+    int off[kPlanCache + 1];
+    int C;
+    int total;
+    long long T, Tf;
+    ChunkDiv cd;            // chunk_div(C) (balanced mode)
+};
+
+__device__ __forceinline__ int plan_split(const Layout &L, const StepArgs &a, int lo, int hi)
+{
+    return a.full_mode ? lo : max(lo, hi - L.band_r);
+}
+
+__device__ __forceinline__ int plan_chunk(const Layout &L, const StepArgs &a, const PlanShared &ps, int nbg, int lo,
+                                          int hi)
+{
+    if (a.plan_mode == 0) return ps.C;
+    const int splits = a.grid_ctas / nbg > 1 ? a.grid_ctas / nbg : 1;
+    return max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
+}
+
+// Up to 32 groups: one warp plans alone -- lane g holds group g, 32 chunk
+// candidates are counted at once (lane k counts candidate k), a ballot picks
+// the smallest that fits, a shuffle scan gives the offsets.
+__device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &ps)
+{
+    const int nbg = a.batch * L.Hkv;
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = 0, sp = 0;
+    if (lane < nbg) {
+        hi = __ldcg(&L.m_cur[lane / L.Hkv]);
+        lo = __ldcg(&L.grp_lo[lane]);
+        sp = plan_split(L, a, lo, hi);
+    }
+    long long T = lane < nbg ? hi - lo : 0, Tf = lane < nbg ? hi : 0;
+    int nseg = lane < nbg ? (sp > lo) + (hi > sp) : 0;
+    for (int o = 16; o; o >>= 1) {
+        T += __shfl_xor_sync(0xffffffffu, T, o);
+        Tf += __shfl_xor_sync(0xffffffffu, Tf, o);
+    }
+    nseg = warp_sum_int(nseg);
+    if (lane < nbg) {
+        ps.lo[lane] = lo;
+        ps.hi[lane] = hi;
+    }
+    __syncwarp();
+    int C = kMinChunk;
+    ChunkDiv RC = {0u, 0};
+    if (a.plan_mode == 0) {
+        const int P = a.grid_ctas;
+        int Q = (4 * nseg <= P) ? P : P * (1 + (2 * nseg + P - 1) / P);
+        if (Q > L.item_cap) Q = L.item_cap;
+        // The smallest fitting chunk is at least T / Q (count(C) >= T / C)
+        // and at most T / (Q - 2 nseg) (count(C) < T / C + 2 nseg).  Float
+        // quotients (relative error < 2^-22) widened by 2^-20 bracket both.
+        const float Tq = (float)T;
+        long long c_lo = (long long)(Tq / (float)Q * (1.f - 0x1p-20f)) / 16 * 16;
+        long long c_hi = Q > 2 * nseg ? round_up16((long long)(Tq / (float)(Q - 2 * nseg) * (1.f + 0x1p-20f)) + 16)
+                                      : (1ll << 30);
+        if (c_lo < kMinChunk) c_lo = kMinChunk;
+        if (c_hi < c_lo) c_hi = c_lo;
+        // candidates c_lo + 16 * stride * k, k = 0..31 (the last one is c_hi)
+        for (;;) {
+            const long long span16 = (c_hi - c_lo) / 16;
+            const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
+            long long cand = c_lo + 16 * stride * lane;
+            if (cand > c_hi) cand = c_hi;
+            const ChunkDiv R = chunk_div((int)cand);
+            int cnt = 0;
+#pragma unroll 4
+            for (int g = 0; g < nbg; g++) {
+                const int glo = ps.lo[g], ghi = ps.hi[g], gsp = plan_split(L, a, glo, ghi);
+                cnt += n_chunks_c(glo, gsp, R) + n_chunks_c(gsp, ghi, R);
+            }
+            const unsigned fit = __ballot_sync(0xffffffffu, cnt <= Q);
+            const int k = fit ? __ffs(fit) - 1 : 31;
+            const long long ck = __shfl_sync(0xffffffffu, cand, k);
+            if (stride == 1 || k == 0) {
+                c_hi = ck;
+                RC.m = __shfl_sync(0xffffffffu, R.m, k);
+                RC.k = __shfl_sync(0xffffffffu, R.k, k);
+                break;
+            }
+            c_hi = ck;   // refine between the previous candidate and this one
+            c_lo = __shfl_sync(0xffffffffu, cand, k - 1) + 16;
+        }
+        C = (int)c_hi;
+    }
+    // per-group counts and offsets
+    int cnt = 0;
+    if (lane < nbg) {
+        if (a.plan_mode == 0) {
+            cnt = n_chunks_c(lo, sp, RC) + n_chunks_c(sp, hi, RC);
+        } else {
+            const int Cg = plan_chunk(L, a, ps, nbg, lo, hi);
+            cnt = n_chunks(lo, sp, Cg) + n_chunks(sp, hi, Cg);
+        }
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, x, 31);
+    if (lane < nbg) ps.off[lane] = x - cnt;
+    if (lane == 0) {
+        ps.off[nbg] = total;
+        ps.total = total < L.item_cap ? total : L.item_cap;
+        ps.C = C;
+        ps.cd = RC;
+        ps.T = T;
+        ps.Tf = Tf;
+    }
+    return true;
+}
+
+__device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
+{
+    const int nbg = a.batch * L.Hkv;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (nbg <= 32) {
+        if (w == 0) cta_plan_small(L, a, ps);
+        __syncthreads();
+        return;
+    }
+    for (int bg = threadIdx.x; bg < nbg; bg += blockDim.x) {
+        ps.hi[bg] = __ldcg(&L.m_cur[bg / L.Hkv]);   // m: the length after this step's append
+        ps.lo[bg] = __ldcg(&L.grp_lo[bg]);
+    }
+    __syncthreads();
+    if (w == 0) {
+        long long T = 0, Tf = 0;
+        int nseg = 0;
+        for (int bg = lane; bg < nbg; bg += 32) {
+            const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
+            T += hi - lo;
+            Tf += hi;
+            nseg += (sp > lo) + (hi > sp);
+        }
+        for (int o = 16; o; o >>= 1) {
+            T += __shfl_xor_sync(0xffffffffu, T, o);
+            Tf += __shfl_xor_sync(0xffffffffu, Tf, o);
+        }
+        nseg = warp_sum_int(nseg);
+        int C = kMinChunk;
+        ChunkDiv RC = chunk_div(kMinChunk);
+        if (a.plan_mode == 0) {
+            auto count = [&](ChunkDiv R) {
+                int c = 0;
+                for (int bg = lane; bg < nbg; bg += 32) {
+                    const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
+                    c += n_chunks_c(lo, sp, R) + n_chunks_c(sp, hi, R);
+                }
+                return warp_sum_int(c);
+            };
+            const long long P = a.grid_ctas;
+            long long Q = (4ll * nseg <= P) ? P : P * (1 + (2ll * nseg + P - 1) / P);
+            if (Q > L.item_cap) Q = L.item_cap;
+            // count(C) < T/C + 2 nseg, so C >= T / (Q - 2 nseg) always fits Q items
+            long long c_lo = round_up16((T + Q - 1) / Q);
+            long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg)) : (1ll << 30);
+            if (c_lo < kMinChunk) c_lo = kMinChunk;
+            if (c_hi < c_lo) c_hi = c_lo;
+            // 32 candidates c_lo + 16 stride k (the last one c_hi, which fits):
+            // lane k forms candidate k's reciprocal (one division for all),
+            // a binary search over k counts the groups once per probe, and
+            // a second round refines between neighbours when stride > 1.
+            for (;;) {
+                const long long span16 = (c_hi - c_lo) / 16;
+                const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
+                long long cand = c_lo + 16 * stride * lane;
+                if (cand > c_hi) cand = c_hi;
+                const ChunkDiv R = chunk_div((int)cand);
+                int k0 = 0, k1 = (int)min(31ll, (span16 + stride - 1) / stride);   // the last distinct candidate
+                while (k0 < k1) {
+                    const int km = (k0 + k1) >> 1;
+                    const ChunkDiv Rm = {__shfl_sync(0xffffffffu, R.m, km), __shfl_sync(0xffffffffu, R.k, km)};
+                    if (count(Rm) <= Q) k1 = km;
+                    else k0 = km + 1;
+                }
+                const long long ck = __shfl_sync(0xffffffffu, cand, k0);
+                const long long cprev = __shfl_sync(0xffffffffu, cand, k0 > 0 ? k0 - 1 : 0);
+                const ChunkDiv Rk = {__shfl_sync(0xffffffffu, R.m, k0), __shfl_sync(0xffffffffu, R.k, k0)};
+                c_hi = ck;
+                if (stride == 1 || k0 == 0) {
+                    RC = Rk;
+                    break;
+                }
+                c_lo = cprev + 16;
+            }
+            C = (int)c_hi;
+        }
+        if (lane == 0) {
+            ps.C = C;
+            ps.cd = RC;
+            ps.T = T;
+            ps.Tf = Tf;
+        }
+    }
+    __syncthreads();
+    // item offsets per group (block scan in rounds keeps the groups in order)
+    int base = 0;
+    for (int r0 = 0; r0 < nbg; r0 += blockDim.x) {
+        const int bg = r0 + threadIdx.x;
+        int cnt = 0;
+        if (bg < nbg) {
+            const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
+            if (a.plan_mode == 0) {
+                cnt = n_chunks_c(lo, sp, ps.cd) + n_chunks_c(sp, hi, ps.cd);
+            } else {
+                const int C = plan_chunk(L, a, ps, nbg, lo, hi);
+                cnt = n_chunks(lo, sp, C) + n_chunks(sp, hi, C);
+            }
+        }
+        int tot;
+        const int off = base + block_exclusive_scan(cnt, &tot);
+        if (bg < nbg) ps.off[bg] = off;
+        base += tot;
+    }
+    if (threadIdx.x == 0) {
+        ps.off[nbg] = base;
+        ps.total = base < L.item_cap ? base : L.item_cap;
+    }
+    __syncthreads();
+}
+
+// Work item `it` of the plan: {group, lo, hi, segment}.
+__device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &ps, int nbg, int it)
+{
+    int g0 = 0, g1 = nbg - 1;   // the last group whose first item is <= it
+    while (g0 < g1) {
+        const int mid = (g0 + g1 + 1) >> 1;
+        if (ps.off[mid] <= it) g0 = mid;
+        else g1 = mid - 1;
+    }
+    const int bg = g0, k = it - ps.off[bg];
+    const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
+    const int C = plan_chunk(L, a, ps, nbg, lo, hi);
+    const ChunkDiv R = a.plan_mode == 0 ? ps.cd : chunk_div(C);
+    const int nA = n_chunks_c(lo, sp, R);
+    if (k < nA) {
+        const int c = div_c(lo, R) + k;
+        return make_int4(bg, max(lo, c * C), min(sp, (c + 1) * C), 0);
+    }
+    const int c = div_c(sp, R) + (k - nA);
+    return make_int4(bg, max(sp, c * C), min(hi, (c + 1) * C), 1);
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV attention.  CTA = NW warps arranged as NP page lanes x NH head
+// tiles (NH = ceil(G/8)); the warps of one page lane share its S-stage
+// shared-memory pipeline of 16-token pages (K 4 KB + V 4 KB, rows XOR
+// swizzled in 16-byte chunks so ldmatrix is conflict-free).
+//
+// Per page and head tile (8 query heads of the group):
+//   S^T[16 tok x 8 heads] = K[16 x 128] Q^T[128 x 8]   8 x mma m16n8k16
+//   online softmax on the fragments (log2 units)
+//   O^T[128 x 8] += V^T[128 x 16] P^T[16 x 8]          8 x 2 mma (P split
+//   into bf16 hi + lo so P V keeps ~16 bits of P: the partials must be
+//   fp32-accurate because Amend's removal amplifies their error)
+//
+// Copy addressing: thread t of a lane group copies the 16-byte chunks
+// t + i * 32 NH of a page; its chunk column is fixed (t mod 16) and its rows
+// step by 2 NH, so every offset is a per-thread constant computed once.
+// ---------------------------------------------------------------------------
+template <int NW, int S, int NH>
+__global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int NP = NW / NH;
+    constexpr int GT = NH * 32;              // threads per page lane
+    constexpr int CPT = 256 / GT;            // 16-byte chunks of K (and of V) per thread per page
+    const int G = L.G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ht = warp % NH, pl = warp / NH;
+    const int gtid = threadIdx.x - pl * GT;
+    uint8_t *lane_smem = smem + (size_t)pl * S * kStageBytes;
+    // comparison build only: the query rows of the head tiles, past the stages and the lane-merge area
+    uint8_t *q_tiles = smem + max((size_t)NP * S * kStageBytes, (size_t)NP * G * kD * 4 + (size_t)NP * G * 8);
+    const uint32_t lane_smem_u32 = smem_u32(lane_smem);
+    const int r4 = lane >> 2, c4 = lane & 3;
+    const float sl2 = L.scale_log2;
+
+    // per-thread copy offsets (bytes within a 4 KB page block / stage half)
+    const int cch = gtid & 15, crow0 = gtid >> 4;   // chunk column, first row
+    uint32_t dst_off[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; i++) {
+        const int row = crow0 + i * (GT / 16);
+        dst_off[i] = row * 256 + ((cch ^ (row & 7)) << 4);
+    }
+    const uint32_t src_off0 = crow0 * 256 + cch * 16;
+    // ldmatrix row bases
+    const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // K tile row (token) this lane addresses
+    const int vtok = (lane & 7) + 8 * (lane >> 4);         // V tile row (token) this lane addresses
+
+    // Q^T fragments of group bg (head column 8 ht + r4) and the band+tail
+    // starts dec_lo of this thread's two head columns (8 ht + 2 c4, + 1).
+    auto load_group = [&](int bg, uint32_t (&qf)[8][2], int &d0, int &d1) {
+        const int b = bg / L.Hkv, g = bg - b * L.Hkv;
+        const size_t hrow = (size_t)b * L.H + (size_t)g * G;
+        const int hn = 8 * ht + r4;
+        if (hn < G) {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.q_post + (hrow + hn) * kD);
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {
+                qf[kk][0] = qrow[8 * kk + c4];
+                qf[kk][1] = qrow[8 * kk + 4 + c4];
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) qf[kk][0] = qf[kk][1] = 0u;
+        }
+        const int hc0 = 8 * ht + 2 * c4;
+        d0 = hc0 < G ? L.dec_lo[hrow + hc0] : 0;
+        d1 = hc0 + 1 < G ? L.dec_lo[hrow + hc0 + 1] : 0;
+    };
+
+    __shared__ PlanShared ps;
+    __shared__ int s_pool[NP][8];   // per page lane: pool pages claimed, by lane step past its own pages
+    pdl_launch_dependents();
+    // Consecutive steps plan almost alike, so this CTA's first item is
+    // likely the one it had in the previous step (a hint only: a stale or
+    // unrelated entry costs bandwidth, never correctness).
+    int spec_bg = -1;
+    if (blockIdx.x < L.item_cap) {
+        const int4 prev = L.items[blockIdx.x];
+        if (prev.x >= 0 && prev.x < a.batch * L.Hkv && prev.y >= 0 && prev.y < prev.z) spec_bg = prev.x;
+    }
+    // While Match runs, HBM is idle: warm L2 with the first pages of that
+    // item (every index is bounds-checked).
+    if (kSpeculativePages > 0 && gtid == 0 && spec_bg >= 0) {
+        const int4 prev = L.items[blockIdx.x];
+        const int pb = prev.x / L.Hkv, pgrp = prev.x - pb * L.Hkv;
+        {
+            for (int k = 0; k < kSpeculativePages; k++) {
+                const int pg = (prev.y >> 4) + pl + k * NP;
+                if (pg * 16 >= prev.z) break;
+                bool ok = true;
+                const size_t off = kv_block(L, pb, pgrp, pg, ok);
+                if (!ok) break;
+                prefetch_l2_bulk(L.k_pool + off, 4096);
+                prefetch_l2_bulk(L.v_pool + off, 4096);
+            }
+        }
+    }
+    pdl_wait();   // spans come from match_plan
+    // the likely first item's queries load while the plan is made
+    uint32_t q_spec[8][2];
+    int d0_spec = 0, d1_spec = 0;
+    if (spec_bg >= 0) load_group(spec_bg, q_spec, d0_spec, d1_spec);
+    cta_plan(L, a, ps);
+    const int nbg = a.batch * L.Hkv;
+    const int n_items = ps.total;
+    if (blockIdx.x == 0) {   // publish the plan for combine and the counters
+        for (int i = threadIdx.x; i <= nbg; i += blockDim.x) L.grp_item_off[i] = min(ps.off[i], n_items);
+        for (int i = threadIdx.x; i < n_items; i += blockDim.x) L.items[i] = plan_item(L, a, ps, nbg, i);
+        if (threadIdx.x == 0) {
+            *L.n_items = n_items;
+            if (ps.off[nbg] > L.item_cap) atomicOr(L.err, kErrPos);
+            atomicAdd(&L.stats[kStSteps], 1ull);
+            atomicAdd(&L.stats[kStKvRead], (unsigned long long)ps.T);
+            atomicAdd(&L.stats[kStKvFull], (unsigned long long)ps.Tf);
+            atomicAdd(&L.stats[kStItems], (unsigned long long)n_items);
+            if (!a.full_mode) atomicAdd(&L.stats[kStDecisions], (unsigned long long)a.batch * L.H);
+        }
+    }
+
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int4 item = plan_item(L, a, ps, nbg, it);
+        const int bg = item.x, ilo = item.y, ihi = item.z;
+        const int b = bg / L.Hkv, g = bg - b * L.Hkv;
+
+        // Q^T fragments for head column n = r4 of this tile
+        uint32_t qf[8][2];
+        int d0, d1;
+        if (it == (int)blockIdx.x && bg == spec_bg) {
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {
+                qf[kk][0] = q_spec[kk][0];
+                qf[kk][1] = q_spec[kk][1];
+            }
+            d0 = d0_spec;
+            d1 = d1_spec;
+        } else {
+            load_group(bg, qf, d0, d1);
+        }
+        if constexpr (kAttnCudaCore) {   // the item's query rows (bf16), 8 per head tile, zeros past G
+            __syncthreads();
+            for (int i = threadIdx.x; i < NH * 8 * 16; i += NW * 32) {
+                const int hh = i >> 4, ch = i & 15;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (hh < G)
+                    v = reinterpret_cast<const uint4 *>(a.q_post + ((size_t)b * L.H + (size_t)g * G + hh) * kD)[ch];
+                reinterpret_cast<uint4 *>(q_tiles)[i] = v;
+            }
+            __syncthreads();
+        }
+        // the item's segment of the group, [slo, shi): any page of it may be
+        // computed here (see the pool below), so masks use its bounds
+        const int glo = ps.lo[bg], ghi = ps.hi[bg], gsp = plan_split(L, a, glo, ghi);
+        const int slo = item.w ? gsp : glo, shi = item.w ? ghi : gsp;
+        // this thread's two head columns and their first valid token (columns
+        // past the group's heads are computed and discarded: no mask)
+        const int hc0 = 8 * ht + 2 * c4, hc1 = hc0 + 1;
+        const int lo0 = max(slo, d0);
+        const int lo1 = max(slo, d1);
+        const int lo_max = max(lo0, lo1);
+
+        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+        float acc[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+        const int pg0 = ilo >> 4, pg1 = (ihi - 1) >> 4;
+        const int npg = pg1 - pg0 + 1;
+
+        // Pages.  Every long item of the segment keeps its last ~8 % of pages
+        // back in a pool shared by the segment's CTAs (not for 32-head
+        // groups, whose CTAs hold a single page lane): a CTA streams its own
+        // other pages (this lane: pg0 + pl + k NP), then claims pool pages one
+        // at a time, so the CTAs of a segment finish together whatever
+        // bandwidth each one gets.  Items of the segment are the C-aligned
+        // chunks c_first, c_first + 1, ... of [slo, shi).
+        constexpr int KDF = NH <= 2 ? kDynFrac : 0;
+        const int Cg = plan_chunk(L, a, ps, nbg, glo, ghi);
+        const ChunkDiv Rg = a.plan_mode == 0 ? ps.cd : chunk_div(Cg);
+        const int c_first = div_c(slo, Rg), n_seg = div_c(shi - 1, Rg) - c_first + 1;
+        auto chunk_pages = [&](int j, int &p0, int &p1) {
+            const int c = c_first + j;
+            p0 = max(slo, c * Cg) >> 4;
+            p1 = (min(shi, (c + 1) * Cg) - 1) >> 4;
+        };
+        auto kept_back = [&](int n) { return (KDF > 0 && n >= kDynMinPages) ? max(2, n * KDF / 128) : 0; };
+        int fp0, fp1, lp0 = 0, lp1 = -1;
+        chunk_pages(0, fp0, fp1);
+        if (n_seg > 1) chunk_pages(n_seg - 1, lp0, lp1);
+        const int a_first = kept_back(fp1 - fp0 + 1);
+        const int a_mid = n_seg > 2 ? kept_back(Cg / 16) : 0;
+        const int a_last = n_seg > 1 ? kept_back(lp1 - lp0 + 1) : 0;
+        const int n_mid = n_seg > 2 ? (n_seg - 2) * a_mid : 0;
+        const int pool = a_first + n_mid + a_last;
+        const int k_self = div_c(ilo, Rg) - c_first;
+        const int kept_self = k_self == 0 ? a_first : (k_self == n_seg - 1 ? a_last : a_mid);
+        const bool dyn = pool > 0 && kept_self > 0;
+        int *const claim_ctr = L.seg_claim + 2 * bg + item.w;
+        // pool slot q -> page (-1 past the pool): the chunks' kept pages in order
+        auto pool_page = [&](int q) -> int {
+            if (q < 0 || q >= pool) return -1;
+            int j = 0, kept = a_first;
+            if (q >= a_first) {
+                q -= a_first;
+                if (q < n_mid) {
+                    j = 1 + q / a_mid;
+                    q -= (j - 1) * a_mid;
+                    kept = a_mid;
+                } else {
+                    j = n_seg - 1;
+                    q -= n_mid;
+                    kept = a_last;
+                }
+            }
+            int p0, p1;
+            chunk_pages(j, p0, p1);
+            return p1 - kept + 1 + q;
+        };
+        const int npg_own = npg - kept_self;
+        const int npl = pl < npg_own ? (npg_own - pl + NP - 1) / NP : 0;   // this lane's own pages
+
+        // L2 prefetch of the page kPrefetchAhead pages past the copy front:
+        // raises the bytes in flight beyond what the shared-memory stages hold
+        auto prefetch = [&](int k) {
+            if (gtid != 0 || k >= npl) return;
+            const int pg = pg0 + pl + k * NP;
+            bool ok = true;
+            const size_t off = kv_block(L, b, g, pg, ok);
+            if (!ok) return;
+            prefetch_l2_bulk(L.k_pool + off, 4096);
+            prefetch_l2_bulk(L.v_pool + off, 4096);
+        };
+        auto issue_page = [&](int pg, int k) {   // page pg into the stage of lane step k
+            const uint32_t st = lane_smem_u32 + (k % S) * kStageBytes;
+            bool ok = true;
+            const size_t off = kv_block(L, b, g, pg, ok);
+            if (!ok) {
+                if (gtid == 0) atomicOr(L.err, kErrPage);
+                return;
+            }
+            const char *ksrc = reinterpret_cast<const char *>(L.k_pool + off) + src_off0;
+            const char *vsrc = reinterpret_cast<const char *>(L.v_pool + off) + src_off0;
+#pragma unroll
+            for (int i = 0; i < CPT; i++) cp_async16(st + dst_off[i], ksrc + i * (GT / 16) * 256);
+#pragma unroll
+            for (int i = 0; i < CPT; i++) cp_async16(st + 4096 + dst_off[i], vsrc + i * (GT / 16) * 256);
+        };
+
+#pragma unroll
+        for (int k = S - 1; k < S - 1 + kPrefetchAhead; k++) prefetch(k);
+#pragma unroll
+        for (int k = 0; k < S - 1; k++) {
+            if (k < npl) issue_page(pg0 + pl + k * NP, k);
+            cp_async_commit();
+        }
+        // lane steps: own pages first, then claimed pool pages; a claim goes
+        // out one step before its page is issued (its result published in
+        // s_pool by the lane's first thread before the step's barrier)
+        int n_iss = min(npl, S - 1);   // pages this lane has issued
+        bool more = dyn;               // the pool may still hold pages for this lane
+        int pend = -2;                 // first thread: the slot claimed last step (-2: none)
+        for (int k = 0; k < n_iss; k++) {
+            cp_async_wait<S - 2>();
+            if (gtid == 0 && pend != -2) {
+                const int pgc = pool_page(pend);
+                s_pool[pl][(n_iss - npl) & 7] = pgc;
+                if (pgc >= 0) {
+                    bool ok = true;
+                    const size_t off = kv_block(L, b, g, pgc, ok);
+                    if (ok) {
+                        prefetch_l2_bulk(L.k_pool + off, 4096);
+                        prefetch_l2_bulk(L.v_pool + off, 4096);
+                    }
+                }
+            }
+            named_bar(1 + pl, GT);
+            if (n_iss == k + S - 1) {
+                int pgn = -1;
+                if (n_iss < npl) {
+                    pgn = pg0 + pl + n_iss * NP;
+                } else if (more) {
+                    pgn = s_pool[pl][(n_iss - npl) & 7];
+                    if (pgn < 0) more = false;
+                }
+                if (pgn >= 0) {
+                    issue_page(pgn, n_iss);
+                    n_iss++;
+                }
+            }
+            cp_async_commit();
+            prefetch(k + S - 1 + kPrefetchAhead);
+            pend = -2;
+            if (gtid == 0 && more && n_iss == k + S && k + S >= npl) pend = atomicAdd(claim_ctr, 1);
+
+            const uint32_t Ks = lane_smem_u32 + (k % S) * kStageBytes;
+            const uint32_t Vs = Ks + 4096;
+            const int pg = k < npl ? pg0 + pl + k * NP : s_pool[pl][(k - npl) & 7];
+
+            // S^T = K Q^T
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (kAttnCudaCore) {
+                const uint8_t *Kp = lane_smem + (k % S) * kStageBytes;
+                const uint8_t *qa = q_tiles + (size_t)(8 * ht + 2 * c4) * 256, *qb = qa + 256;
+                const int ra = r4, rb = r4 + 8;
+#pragma unroll 4
+                for (int ch = 0; ch < 16; ch++) {
+                    const uint4 ka = *reinterpret_cast<const uint4 *>(Kp + ra * 256 + ((ch ^ (ra & 7)) << 4));
+                    const uint4 kb = *reinterpret_cast<const uint4 *>(Kp + rb * 256 + ((ch ^ (rb & 7)) << 4));
+                    const uint4 q0 = *reinterpret_cast<const uint4 *>(qa + ch * 16);
+                    const uint4 q1 = *reinterpret_cast<const uint4 *>(qb + ch * 16);
+                    dot8_bf16(s[0], ka, q0);
+                    dot8_bf16(s[1], ka, q1);
+                    dot8_bf16(s[2], kb, q0);
+                    dot8_bf16(s[3], kb, q1);
+                }
+            } else {
+                const uint32_t rbase = Ks + krow * 256;
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    const int ch = 2 * kk + (lane >> 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(a0, a1, a2, a3, rbase + ((ch ^ (krow & 7)) << 4));
+                    mma_bf16(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                }
+            }
+            // s[0]: token r4 head hc0; s[1]: token r4 head hc1; s[2], s[3]: token r4+8
+            float z0 = s[0] * sl2, z1 = s[1] * sl2, z2 = s[2] * sl2, z3 = s[3] * sl2;
+            if (pg * 16 < lo_max || pg * 16 + 16 > shi) {
+                const int j0 = pg * 16 + r4, j1 = j0 + 8;
+                if (!(j0 >= lo0 && j0 < shi)) z0 = -CUDART_INF_F;
+                if (!(j0 >= lo1 && j0 < shi)) z1 = -CUDART_INF_F;
+                if (!(j1 >= lo0 && j1 < shi)) z2 = -CUDART_INF_F;
+                if (!(j1 >= lo1 && j1 < shi)) z3 = -CUDART_INF_F;
+            }
+            float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float bs0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+            const float bs1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+            const float p0 = exp2f(z0 - bs0), p1 = exp2f(z1 - bs1);
+            const float p2 = exp2f(z2 - bs0), p3 = exp2f(z3 - bs1);
+            // rescale only when some running max moved (rare after the first pages)
+            if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+                const float al0 = exp2f(m0 - bs0), al1 = exp2f(m1 - bs1);
+                l0 *= al0;
+                l1 *= al1;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    acc[i][0] *= al0;
+                    acc[i][1] *= al1;
+                    acc[i][2] *= al0;
+                    acc[i][3] *= al1;
+                }
+            }
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            m0 = mn0;
+            m1 = mn1;
+            if constexpr (kAttnCudaCore) {   // O^T += V^T P^T with fp32 P gathered from the lanes that hold it
+                const uint8_t *Vp = lane_smem + (k % S) * kStageBytes + 4096;
+#pragma unroll 2
+                for (int t = 0; t < 16; t++) {
+                    const int src = (t & 7) * 4 + c4;
+                    const float pa = __shfl_sync(0xffffffffu, t < 8 ? p0 : p2, src);
+                    const float pb = __shfl_sync(0xffffffffu, t < 8 ? p1 : p3, src);
+                    const uint8_t *vrow = Vp + t * 256 + r4 * 2;
+#pragma unroll
+                    for (int mt = 0; mt < 8; mt++) {
+                        const float v0 = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(
+                                                             vrow + (((2 * mt) ^ (t & 7)) << 4)) << 16);
+                        const float v1 = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(
+                                                             vrow + (((2 * mt + 1) ^ (t & 7)) << 4)) << 16);
+                        acc[mt][0] = fmaf(v0, pa, acc[mt][0]);
+                        acc[mt][1] = fmaf(v0, pb, acc[mt][1]);
+                        acc[mt][2] = fmaf(v1, pa, acc[mt][2]);
+                        acc[mt][3] = fmaf(v1, pb, acc[mt][3]);
+                    }
+                }
+                continue;
+            }
+            // P^T fragments (hi + lo bf16 parts) via in-register transpose
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+            const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+            const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+            const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+            const uint32_t bh0 = movmatrix_t(bf16x2_bits(h01)), bh1 = movmatrix_t(bf16x2_bits(h23));
+            const uint32_t bl0 = movmatrix_t(bf16x2_bits(e01)), bl1 = movmatrix_t(bf16x2_bits(e23));
+            {
+                const uint32_t vbase = Vs + vtok * 256;
+#pragma unroll
+                for (int mt = 0; mt < 8; mt++) {
+                    const int ch = 2 * mt + ((lane >> 3) & 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(a0, a1, a2, a3, vbase + ((ch ^ (vtok & 7)) << 4));
+                    mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
+                    mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
+                }
+            }
+        }
+        cp_async_wait<0>();
+        __syncthreads();   // every page lane drained: stage memory is free
+
+        // sum l over the 8 lanes that share a head column
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        }
+        if constexpr (NP == 1) {   // one page lane: the fragments are the item's partial
+            const float NEG = -CUDART_INF_F;
+            if (hc0 < G) {
+                float *o0 = L.part_o + ((size_t)it * G + hc0) * kD;
+                const bool none = m0 == NEG;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    o0[16 * i + r4] = none ? 0.f : acc[i][0];
+                    o0[16 * i + r4 + 8] = none ? 0.f : acc[i][2];
+                }
+                if (r4 == 0) L.part_ml[(size_t)it * G + hc0] = make_float2(m0, none ? 0.f : l0);
+            }
+            if (hc1 < G) {
+                float *o1 = L.part_o + ((size_t)it * G + hc1) * kD;
+                const bool none = m1 == NEG;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    o1[16 * i + r4] = none ? 0.f : acc[i][1];
+                    o1[16 * i + r4 + 8] = none ? 0.f : acc[i][3];
+                }
+                if (r4 == 0) L.part_ml[(size_t)it * G + hc1] = make_float2(m1, none ? 0.f : l1);
+            }
+            continue;   // the stage memory was drained above; nothing else is staged
+        }
+        // stage each page lane's partial in shared memory, then merge lanes
+        float *red_o = reinterpret_cast<float *>(smem);                               // [NP][G][D]
+        float2 *red_ml = reinterpret_cast<float2 *>(red_o + (size_t)NP * G * kD);     // [NP][G]
+        if (hc0 < G) {
+            float *o0 = red_o + ((size_t)pl * G + hc0) * kD;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                o0[16 * i + r4] = acc[i][0];
+                o0[16 * i + r4 + 8] = acc[i][2];
+            }
+            if (r4 == 0) red_ml[pl * G + hc0] = make_float2(m0, l0);
+        }
+        if (hc1 < G) {
+            float *o1 = red_o + ((size_t)pl * G + hc1) * kD;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                o1[16 * i + r4] = acc[i][1];
+                o1[16 * i + r4 + 8] = acc[i][3];
+            }
+            if (r4 == 0) red_ml[pl * G + hc1] = make_float2(m1, l1);
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < G * kD; idx += NW * 32) {
+            const int hh = idx / kD, dd = idx - hh * kD;
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int q = 0; q < NP; q++) M = fmaxf(M, red_ml[q * G + hh].x);
+            float lsum = 0.f, osum = 0.f;
+            if (M != -CUDART_INF_F) {
+#pragma unroll
+                for (int q = 0; q < NP; q++) {
+                    const float2 ml = red_ml[q * G + hh];
+                    const float wq = exp2f(ml.x - M);
+                    lsum += ml.y * wq;
+                    osum += red_o[((size_t)q * G + hh) * kD + dd] * wq;
+                }
+            }
+            L.part_o[((size_t)it * G + hh) * kD + dd] = osum;
+            if (dd == 0) L.part_ml[(size_t)it * G + hh] = make_float2(M, lsum);
+        }
+        __syncthreads();   // shared memory is reused by the next item's pipeline
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+static int head_tiles(int G) { return (G + 7) / 8; }
+
+static size_t attention_smem(int G)
+{
+    const int NH = head_tiles(G), NP = kAttnWarps / NH;
+    const size_t pipe = (size_t)NP * kAttnStages * kStageBytes;
+    const size_t red = (size_t)NP * G * kD * 4 + (size_t)NP * G * 8;
+    const size_t q_tiles = kAttnCudaCore ? (size_t)NH * 8 * kD * 2 : 0;   // after the stages
+    return (pipe > red ? pipe : red) + q_tiles;
+}
+
+template <int NH>
+static cudaError_t attention_config_nh(size_t smem, int *ctas_per_sm)
+{
+    auto k = attention_kernel<kAttnWarps, kAttnStages, NH>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, k, kAttnWarps * 32, smem);
+}
+
+cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm)
+{
+    *smem = attention_smem(G);
+    switch (head_tiles(G)) {
+    case 1: return attention_config_nh<1>(*smem, ctas_per_sm);
+    case 2: return attention_config_nh<2>(*smem, ctas_per_sm);
+    default: return attention_config_nh<4>(*smem, ctas_per_sm);
+    }
+}
+
+
+
+cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)
+{
+    const dim3 grid(a.grid_ctas), block(kAttnWarps * 32);
+    switch (head_tiles(L.G)) {
+    case 1: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1>, grid, block, smem, s, a.pdl, L, a);
+    case 2: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2>, grid, block, smem, s, a.pdl, L, a);
+    default: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 4>, grid, block, smem, s, a.pdl, L, a);
+    }
+}
+
+}  // namespace macgpu
