@@ -167,6 +167,19 @@ mac_status mac_decode_step(mac_handle h, int batch, const void *dev_q_pre, const
                            const void *dev_k_new, const void *dev_v_new, void *dev_out, float *dev_lse_out,
                            void *stream);
 
+/* mac_decode_step with its inputs and results in page-locked host memory
+ * (cudaHostAlloc / cudaMallocHost / cudaHostRegister; same layouts as
+ * above): the step's kernels read q_pre, q_post, k_new and v_new and write
+ * out and lse_out in place over the host link (NVLink-C2C on Grace
+ * systems), so the transfers ride inside the step's three launches instead
+ * of separate copies.  The host buffers must stay untouched until the work
+ * on `stream` is complete; results are valid after a stream/event sync.
+ * MAC_ERR_INVALID_ARG if a buffer is not page-locked host memory the device
+ * can address (pageable memory is refused, not staged).  Async on stream. */
+mac_status mac_decode_step_host(mac_handle h, int batch, const void *host_q_pre, const void *host_q_post,
+                                const void *host_k_new, const void *host_v_new, void *host_out,
+                                float *host_lse_out, void *stream);
+
 /* Full split-KV decode attention (the miss path for every head; no Match,
  * no ring update): append, then out = AS_{1:m}(q_post).  The in-library
  * baseline the MAC path is compared against.  Async on stream. */

@@ -49,6 +49,7 @@ SIGNATURES = {
     "mac_set_page_table": (_i, [_vp, _i, _vp, _i, _vp]),
     "mac_append_kv": (_i, [_vp, _i, _vp, _vp, _i64, _vp]),
     "mac_decode_step": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mac_decode_step_host": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mac_full_step": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mac_join": (_i, [_vp, _vp]),
     "mac_sync": (_i, [_vp, _i]),

@@ -41,6 +41,18 @@ def _dev(t: torch.Tensor, name, dtype, shape=None, device=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _host(t: torch.Tensor, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise TypeError(f"{name} must be a pinned (page-locked) CPU tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def make_config(heads, kv_heads, head_dim, ring_len, band_r, tau, max_batch, max_ctx, page_size=16,
                 num_pages=0, sm_scale=0.0, plan_mode=0, amend_band=0) -> N.MacConfig:
     return N.MacConfig(heads, kv_heads, head_dim, ring_len, band_r, float(tau), max_batch, int(max_ctx),
@@ -154,6 +166,21 @@ class MacAttention:
                                      _dev(out, "out", torch.bfloat16, qs, device=self.device), lp,
                                      _stream_ptr(stream, self.device))
         _check("mac_decode_step", st, self._h)
+        return out, lse
+
+    def decode_step_host(self, q_pre, q_post, k_new, v_new, out, lse=None, stream=None):
+        """decode_step with pinned host tensors: the step's kernels read the
+        inputs and write out (and lse) in place in host memory; the results
+        are valid once `stream` has been synchronised."""
+        B = q_pre.shape[0]
+        qs, ks = (B, self.heads, self.head_dim), (B, self.kv_heads, self.head_dim)
+        lp = _host(lse, "lse", torch.float32, (B, self.heads)) if lse is not None else ctypes.c_void_p(None)
+        st = N.lib().mac_decode_step_host(self._h, B, _host(q_pre, "q_pre", torch.bfloat16, qs),
+                                          _host(q_post, "q_post", torch.bfloat16, qs),
+                                          _host(k_new, "k_new", torch.bfloat16, ks),
+                                          _host(v_new, "v_new", torch.bfloat16, ks),
+                                          _host(out, "out", torch.bfloat16, qs), lp, _stream_ptr(stream, self.device))
+        _check("mac_decode_step_host", st, self._h)
         return out, lse
 
     def full_step(self, q_post, k_new, v_new, out=None, lse=None, want_lse=True, stream=None):

@@ -262,7 +262,7 @@ mac_status prof_collect(mac_ctx *h)
 
 // The step chain shared by mac_decode_step and mac_full_step.
 mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post, const void *k_new,
-                    const void *v_new, void *out, float *lse_out, void *stream, bool full)
+                    const void *v_new, void *out, float *lse_out, void *stream, bool full, bool host_io = false)
 {
     mac_status st = check_handle(h);
     if (st != MAC_OK) return st;
@@ -309,7 +309,13 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
         MAC_CUDA(h, launch_match_plan(h->lay, am, s));
     }
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[1], s));
-    MAC_CUDA(h, launch_attention(h->lay, a, h->attn_smem, s));
+    {
+        // inputs in host memory: the attention kernel takes the queries
+        // from the device copy Match keeps (q_stash, same layout)
+        StepArgs aa = a;
+        if (host_io) aa.q_post = h->lay.q_stash;
+        MAC_CUDA(h, launch_attention(h->lay, aa, h->attn_smem, s));
+    }
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[2], s));
     MAC_CUDA(h, launch_combine(h->lay, a, s));
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[3], s));
@@ -554,6 +560,36 @@ mac_status mac_decode_step(mac_handle h, int batch, const void *dev_q_pre, const
                            void *stream)
 {
     return run_step(h, batch, dev_q_pre, dev_q_post, dev_k_new, dev_v_new, dev_out, dev_lse_out, stream, false);
+}
+
+// The device's address of page-locked host memory (the same address under
+// unified addressing); nullptr for anything else.
+static void *host_for_device(const void *p)
+{
+    if (!p) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+mac_status mac_decode_step_host(mac_handle h, int batch, const void *host_q_pre, const void *host_q_post,
+                                const void *host_k_new, const void *host_v_new, void *host_out,
+                                float *host_lse_out, void *stream)
+{
+    const mac_status st = check_handle(h);
+    if (st != MAC_OK) return st;
+    const void *q_pre = host_for_device(host_q_pre), *q_post = host_for_device(host_q_post);
+    const void *k_new = host_for_device(host_k_new), *v_new = host_for_device(host_v_new);
+    void *out = host_for_device(host_out);
+    float *lse = (float *)host_for_device(host_lse_out);
+    if (!q_pre || !q_post || !k_new || !v_new || !out || (host_lse_out && !lse)) {
+        std::snprintf(h->errbuf, sizeof h->errbuf, "a host buffer is not page-locked memory the device can address");
+        return MAC_ERR_INVALID_ARG;
+    }
+    return run_step(h, batch, q_pre, q_post, k_new, v_new, out, lse, stream, false, true);
 }
 
 mac_status mac_full_step(mac_handle h, int batch, const void *dev_q_post, const void *dev_k_new,

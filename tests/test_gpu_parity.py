@@ -262,3 +262,53 @@ def test_wide_ring_seeded_from_prefill(ring_len, n_seed):
         ref, _ = p.mac_step(t, force=True, check_ring=(t == c.steps - 1))
         hits += int(ref["hit"].sum())
     assert hits > 0
+
+
+def test_host_buffer_step_is_the_device_step():
+    """mac_decode_step_host -- inputs and results in pinned host memory, read
+    and written in place by the step's kernels -- gives bitwise the outputs,
+    LSEs, decisions and rings of mac_decode_step on the same inputs; the
+    device path itself is checked against the oracle step by step."""
+    from gpu_harness import check_out, KEYS
+    c = cfg(steps=12, rho=0.995, ring_len=8)
+    pd, ph = _pair(c), _pair(c)
+    B, H, d = c.batch, c.heads, c.head_dim
+    h_out = torch.empty((B, H, d), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    for t in range(c.steps):
+        dev, host = pd.step_inputs(t)
+        ref = pd.orc.step(*host)
+        out_d, lse_d = pd.mac.decode_step(*dev)
+        h_in = [ph.inputs[k][t].contiguous().pin_memory() for k in KEYS]
+        ph.mac.decode_step_host(*h_in, out=h_out, lse=h_lse)
+        torch.cuda.synchronize()
+        check_out(out_d, lse_d, ref, f"step {t}")
+        assert torch.equal(out_d.cpu().view(torch.int16), h_out.view(torch.int16)), f"step {t}: out differs"
+        assert torch.equal(lse_d.cpu(), h_lse), f"step {t}: lse differs"
+        dd, dh = pd.mac.decisions(B), ph.mac.decisions(B)
+        for k in dd:
+            np.testing.assert_array_equal(dd[k], dh[k])
+    for b in range(B):
+        rd, rh = pd.mac.read_ring(b), ph.mac.read_ring(b)
+        for k in rd:
+            np.testing.assert_array_equal(np.asarray(rd[k]), np.asarray(rh[k]))
+    assert ph.mac.stats()["hits"] > 0 and ph.mac.stats()["device_error"] == 0
+
+
+def test_host_buffer_step_refuses_pageable_memory():
+    """Pageable host memory is refused before any launch: by the binding, and
+    by the C entry point itself (MAC_ERR_INVALID_ARG, no step taken)."""
+    import ctypes
+    from gpu_harness import KEYS
+    from kv_cache_computation_gb300 import _native as N
+    c = cfg(steps=1)
+    p = _pair(c)
+    args = [p.inputs[k][0].contiguous() for k in KEYS]
+    out = torch.empty((c.batch, c.heads, c.head_dim), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        p.mac.decode_step_host(*args, out=out)
+    ptrs = [ctypes.c_void_p(a.data_ptr()) for a in args]
+    st = N.lib().mac_decode_step_host(p.mac._h, c.batch, *ptrs, ctypes.c_void_p(out.data_ptr()), None, None)
+    assert st == -1
+    torch.cuda.synchronize()
+    assert p.mac.stats()["steps"] == 0
