@@ -264,14 +264,16 @@ def test_wide_ring_seeded_from_prefill(ring_len, n_seed):
     assert hits > 0
 
 
-def test_host_buffer_step_is_the_device_step():
+@pytest.mark.parametrize("amend_band", [0, 1])
+def test_host_buffer_step_is_the_device_step(amend_band):
     """mac_decode_step_host -- inputs and results in pinned host memory, read
     and written in place by the step's kernels -- gives bitwise the outputs,
-    LSEs, decisions and rings of mac_decode_step on the same inputs; the
-    device path itself is checked against the oracle step by step."""
+    LSEs, decisions and rings of mac_decode_step on the same inputs, with
+    Amend in the merge epilogue or on the side stream; the device path
+    itself is checked against the oracle step by step."""
     from gpu_harness import check_out, KEYS
     c = cfg(steps=12, rho=0.995, ring_len=8)
-    pd, ph = _pair(c), _pair(c)
+    pd, ph = _pair(c, amend_band=amend_band), _pair(c, amend_band=amend_band)
     B, H, d = c.batch, c.heads, c.head_dim
     h_out = torch.empty((B, H, d), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
@@ -281,6 +283,8 @@ def test_host_buffer_step_is_the_device_step():
         out_d, lse_d = pd.mac.decode_step(*dev)
         h_in = [ph.inputs[k][t].contiguous().pin_memory() for k in KEYS]
         ph.mac.decode_step_host(*h_in, out=h_out, lse=h_lse)
+        pd.mac.sync()
+        ph.mac.sync()
         torch.cuda.synchronize()
         check_out(out_d, lse_d, ref, f"step {t}")
         assert torch.equal(out_d.cpu().view(torch.int16), h_out.view(torch.int16)), f"step {t}: out differs"
