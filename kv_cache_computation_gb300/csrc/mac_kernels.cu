@@ -359,8 +359,9 @@ __device__ __forceinline__ bool remove_band(float lf, float4 of, float lb, float
 
 // KB partials per warp per round of loads: 4, or 16 when a group may hold
 // hundreds of items (one request's single KV group spread over the grid).
-// NW warps per block: kCombineWarps, or 2 when every head has a handful of
-// items (many requests, where the grid is thousands of blocks).
+// NW warps per block: kCombineWarps, or one warp taking every item in one
+// round when each head has a handful of items (many requests, where the
+// grid is thousands of blocks).
 constexpr int kCombineWarps = 8;
 
 template <int KB, int NW>
@@ -735,7 +736,7 @@ cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
     const dim3 grid(a.batch * L.H);
     // A few items per head (many requests): small blocks, so that the whole
     // grid is resident beside the attention CTAs when their wait releases.
-    if (per_group <= 8) return launch_maybe_pdl(combine_kernel<4, 2>, grid, dim3(64), 0, s, a.pdl != 0, L, a);
+    if (per_group <= 8) return launch_maybe_pdl(combine_kernel<8, 1>, grid, dim3(32), 0, s, a.pdl != 0, L, a);
     const dim3 block(kCombineWarps * 32);
     if (per_group > 128) return launch_maybe_pdl(combine_kernel<16, kCombineWarps>, grid, block, 0, s, a.pdl != 0, L, a);
     return launch_maybe_pdl(combine_kernel<4, kCombineWarps>, grid, block, 0, s, a.pdl != 0, L, a);
