@@ -103,6 +103,7 @@ def test_create_checks_buffers_before_touching_the_gpu(native):
 def test_null_handle_calls_fail_cleanly(native):
     L = native.lib()
     assert L.mac_decode_step(None, 1, None, None, None, None, None, None, None) == -1
+    assert L.mac_decode_step_host(None, 1, None, None, None, None, None, None, None) == -1
     assert L.mac_sync(None, 0) == -1
     assert L.mac_destroy(None) == -1
     assert L.mac_last_error(None) == b""
@@ -114,3 +115,20 @@ def test_status_strings(native):
         s = L.mac_status_string(code)
         assert s and s != b"unknown status"
     assert L.mac_status_string(5) == b"unknown status"
+
+
+def test_host_binding_refuses_what_the_kernels_cannot_address():
+    """The host-buffer binding takes pinned CPU tensors only: pageable memory,
+    a wrong dtype or shape is refused before anything reaches the library."""
+    import torch
+    from kv_cache_computation_gb300.attention import _host
+    t = torch.zeros((2, 4, 128), dtype=torch.bfloat16)   # pageable
+    with pytest.raises(TypeError, match="pinned"):
+        _host(t, "q_pre", torch.bfloat16, (2, 4, 128))
+    if torch.cuda.is_available():
+        p = t.pin_memory()
+        assert _host(p, "q_pre", torch.bfloat16, (2, 4, 128)).value == p.data_ptr()
+        with pytest.raises(TypeError):
+            _host(p, "q_pre", torch.float32)
+        with pytest.raises(ValueError):
+            _host(p, "q_pre", torch.bfloat16, (2, 4, 64))
