@@ -39,25 +39,26 @@ def check_out(out, lse, ref, what=""):
 _PREFILL_CACHE = {}
 
 
-def prefill(cfg):
-    """Prefill K, V for a workload (CPU), cached across tests that share them."""
-    key = (cfg.seed, cfg.batch, cfg.context, cfg.kv_heads, cfg.head_dim, cfg.rope_base,
+def prefill(cfg, layer=0):
+    """Prefill K, V for a workload layer (CPU), cached across tests that share them."""
+    key = (cfg.seed, layer, cfg.batch, cfg.context, cfg.kv_heads, cfg.head_dim, cfg.rope_base,
            tuple(cfg.channel_scale_range or ()))
     if key not in _PREFILL_CACHE:
         _PREFILL_CACHE.clear()
-        _PREFILL_CACHE[key] = W.prefill_kv(cfg)
+        _PREFILL_CACHE[key] = W.prefill_kv(cfg, layer=layer)
     return _PREFILL_CACHE[key]
 
 
 class Pair:
     """A MAC handle and the oracle over identical inputs."""
 
-    def __init__(self, cfg: W.DecodeConfig, contexts=None, page_size=16, plan_mode=0, extra_steps=0, amend_band=0):
+    def __init__(self, cfg: W.DecodeConfig, contexts=None, page_size=16, plan_mode=0, extra_steps=0, amend_band=0,
+                 layer=0):
         self.cfg = cfg
         B = cfg.batch
         self.contexts = list(contexts) if contexts is not None else [cfg.context] * B
         self.t_max = max(self.contexts) + cfg.steps + extra_steps
-        K, V = prefill(cfg) if cfg.context > 0 else (None, None)
+        K, V = prefill(cfg, layer) if cfg.context > 0 else (None, None)
         self.mac = MacAttention(cfg.heads, cfg.kv_heads, cfg.head_dim, cfg.ring_len, cfg.band_r, cfg.tau,
                                 max_batch=B, max_ctx=self.t_max, page_size=page_size, plan_mode=plan_mode,
                                 amend_band=amend_band)
@@ -76,7 +77,7 @@ class Pair:
         self.orc = oracle.MacState(Ko, Vo, cfg.heads, cfg.ring_len, cfg.band_r, cfg.tau)
         for b, n in enumerate(self.contexts):
             self.orc.reset(b, n)
-        self.inputs = W.decode_inputs(cfg)
+        self.inputs = W.decode_inputs(cfg, layer=layer)
         self.flagged = 0
 
     def step_inputs(self, t):

@@ -23,9 +23,9 @@ def _built():
     build.build()
 
 
-def _run(cfg, steps, page_size, ring_every=8):
+def _run(cfg, steps, page_size, ring_every=8, layer=0):
     from gpu_harness import Pair
-    p = Pair(cfg, page_size=page_size)
+    p = Pair(cfg, page_size=page_size, layer=layer)
     hits = 0
     for t in range(steps):
         ref, _ = p.mac_step(t, force=True, check_ring=(t % ring_every == ring_every - 1))
@@ -55,11 +55,13 @@ def test_llama_128k_heterogeneous_rho(band_r):
     assert hits > 0
 
 
-def test_qwen_stack_layer_4x120k_hits():
-    """One layer of the 48-layer stack at full size (4 x 122880, 32 q / 4 KV
-    heads, per-channel K/V scales), tau 0.45 so heads hit and miss."""
-    cfg = W.qwen_moe_stack_120k_b4(steps=12, tau=0.45, layers=1)
-    p, hits = _run(cfg, 12, page_size=16, ring_every=6)
+@pytest.mark.parametrize("layer", [0, 47])
+def test_qwen_stack_layer_4x120k_hits(layer):
+    """The first and the last layer of the 48-layer stack at full size
+    (4 x 122880, 32 q / 4 KV heads, the layer's own per-channel K/V scales
+    and query streams), tau 0.45 so heads hit and miss."""
+    cfg = W.qwen_moe_stack_120k_b4(steps=12, tau=0.45, layers=48)
+    p, hits = _run(cfg, 12, page_size=16, ring_every=6, layer=layer)
     assert hits > 0
 
 
