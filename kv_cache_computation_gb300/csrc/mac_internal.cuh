@@ -12,8 +12,8 @@ namespace macgpu {
 constexpr int kD = 128;                 // head_dim
 constexpr int kPage = 16;               // tokens per KV page / per staged block
 constexpr int kMaxRing = 4096;          // ring entries per (request, head)
-constexpr int kSmallRing = 32;          // rings up to this size (one entry per lane) are scanned inside
-                                        // the Match kernel, for groups of up to 16 heads
+constexpr int kSmallRing = 32;          // rings up to this size (one entry's distance per lane) are
+                                        // scanned inside the Match kernel
 constexpr int kScanBlock = 256;         // ring entries per block of the wide-ring scan
 constexpr int kMaxGroup = 32;           // query heads per KV head
 constexpr int kMatchWarps = 8;          // query heads (warps) per Match block at most
