@@ -64,3 +64,23 @@ def test_reference_arm_runs_on_rank0_only():
     class A:
         steps, warmup, workload, band_r, ref_budget = 2, 3, "gqa_4k_b1_contig", 64, 5.0
     assert bench.bench_reference(A(), 2, 1, 1) is None
+
+
+def test_launch_count_and_traffic_provenance(tmp_path):
+    """bench.py's claims about itself: a decode step is three launches, four
+    with the grid-wide ring scan (rings over 32 entries) and one more with the
+    side-stream Amend; the ncu traffic figure is used only while the hash of
+    the attention kernel's sources matches the one the summary records."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from types import SimpleNamespace as NS
+    assert bench.launches_per_step(NS(ring_len=16, group=32), 0) == 3
+    assert bench.launches_per_step(NS(ring_len=32, group=4), 0) == 3
+    assert bench.launches_per_step(NS(ring_len=33, group=4), 0) == 4
+    assert bench.launches_per_step(NS(ring_len=1024, group=32), 1) == 5
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    h1 = bench.kernel_source_sha([str(src)])
+    src.write_text("kernel v2")
+    assert bench.kernel_source_sha([str(src)]) != h1 and len(h1) == 16
+    assert any(f.endswith("mac_attention.cu") for f in bench.KERNEL_SOURCES)
