@@ -168,8 +168,8 @@ mac_status mac_decode_step(mac_handle h, int batch, const void *dev_q_pre, const
                            void *stream);
 
 /* mac_decode_step with its inputs and results in page-locked host memory
- * (cudaHostAlloc / cudaMallocHost / cudaHostRegister; same layouts as
- * above): the step's kernels read q_pre, q_post, k_new and v_new and write
+ * (cudaHostAlloc / cudaMallocHost / cudaHostRegister; same layouts and
+ * alignment as above): the step's kernels read q_pre, q_post, k_new and v_new and write
  * out and lse_out in place over the host link (NVLink-C2C on Grace
  * systems), so the transfers ride inside the step's three launches instead
  * of separate copies.  The host buffers must stay untouched until the work
