@@ -156,3 +156,55 @@ def test_mac_steps_match_brute_force(B, H, Hkv, L, r, tau):
 def _tolist_kv(A):
     return [[[[float(x) for x in bf16_value(A[b, t, g])] for g in range(A.shape[2])]
              for t in range(A.shape[1])] for b in range(A.shape[0])]
+
+
+def test_band_holding_the_mass_takes_the_direct_form():
+    """Removal is ill-conditioned when the band [m-r+1, m] carries almost all
+    of AS_{1:m}'s mass (1 - e^delta near 0): the stored summary is then
+    formed directly as the merge of its parts.  Each new key is a growing
+    multiple of the (fixed) post-RoPE query direction, so the newest token's
+    score exceeds every older one by 20: the prefix [1, m-r] holds about
+    e^-40 of the mass.  The ring entry must still equal AS_{1:m-r} built from
+    its token set, on hit steps (reused prefix merged with [p-r+1, m-r]) and
+    on miss steps (tokens [1, m-r])."""
+    B, H, Hkv, d, L, r, tau, scale = 1, 2, 1, 4, 3, 2, 0.3, 0.5
+    ctx, steps = 3, 8
+    rng = np.random.default_rng(2604)
+    t_max = ctx + steps
+    K = np.zeros((B, t_max, Hkv, d), np.uint16)
+    V = np.zeros((B, t_max, Hkv, d), np.uint16)
+    K[:, :ctx] = bits(rng.standard_normal((B, ctx, Hkv, d)))
+    V[:, :ctx] = bits(rng.standard_normal((B, ctx, Hkv, d)))
+    st = oracle.MacState(K, V, H, L, r, tau, scale)
+    st.reset(0, ctx)
+    bf = BruteMac(_tolist_kv(K[:, :ctx]), _tolist_kv(V[:, :ctx]), H, L, r, tau, scale)
+    u = np.ones(d)
+    q_post = bits(np.stack([u, 0.75 * u])[None])               # [1, H, d]: scores 2 alpha and 1.5 alpha
+    qt = rng.standard_normal((B, H, d))
+    reuse = {1, 2, 4, 5, 7}                                    # steps whose pre-RoPE query barely moves
+    hit_steps = miss_steps = 0
+    for t in range(steps):
+        qt = qt + 0.01 * rng.standard_normal(qt.shape) if t in reuse else rng.standard_normal(qt.shape)
+        q_pre = bits(qt)
+        k_new = bits((10.0 * (t + 1)) * u[None, None])         # alpha_t = 10 (t + 1)
+        v_new = bits(rng.standard_normal((B, Hkv, d)))
+        before = st.direct_count
+        got = st.step(q_pre, q_post, k_new, v_new)
+        exp = bf.step(_tolist(bf16_value(q_pre)), _tolist(bf16_value(q_post)),
+                      _tolist(bf16_value(k_new)), _tolist(bf16_value(v_new)))
+        m = ctx + t + 1
+        ring = st.ring()
+        slot = t % L
+        for h in range(H):
+            e = exp[0][h]
+            assert bool(got["hit"][0, h]) == e["hit"], (t, h)
+            np.testing.assert_allclose(got["out"][0, h], e["out"][0], rtol=0, atol=1e-12)
+            ent = e["ent"]["AS"]
+            np.testing.assert_allclose(ring["o"][0, h, slot], ent[0], rtol=0, atol=1e-11)
+            assert ring["lse"][0, h, slot] == pytest.approx(ent[1], abs=1e-11)
+            if m > r:
+                hit_steps += e["hit"]
+                miss_steps += not e["hit"]
+        if m > r:
+            assert st.direct_count - before == H, f"step {t}: the removal should have been ill-conditioned"
+    assert hit_steps > 0 and miss_steps > 0

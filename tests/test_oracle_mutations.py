@@ -38,6 +38,15 @@ MUTANTS = {
     "ring_slot_shift": ("const long slot_new = (long)(s->step[b] % L);",
                         "const long slot_new = (long)((s->step[b] + 1) % L);"),
     "kv_head_index": ("g = h / G;\n        if (h < h_lo", "g = h % s->Hkv;\n        if (h < h_lo"),
+    "direct_miss_range_to_m": ("orc_attention_summary(q, Kh, Vh, row, 0, m - r, d, s->scale, oe, &le);",
+                               "orc_attention_summary(q, Kh, Vh, row, 0, m, d, s->scale, oe, &le);"),
+    "direct_hit_range_to_m": ("orc_attention_summary(q, Kh, Vh, row, lo, m - r, d, s->scale, ot, &lt);",
+                              "orc_attention_summary(q, Kh, Vh, row, lo, m, d, s->scale, ot, &lt);"),
+    "direct_hit_range_from_0": ("orc_attention_summary(q, Kh, Vh, row, lo, m - r, d, s->scale, ot, &lt);",
+                                "orc_attention_summary(q, Kh, Vh, row, 0, m - r, d, s->scale, ot, &lt);"),
+    "direct_hit_prefix_dropped": ("orc_merge(s->ring_o + (ring_base + e) * d, s->ring_lse[ring_base + e], ot, lt, d, oe, &le);",
+                                  "memcpy(oe, ot, (size_t)d * sizeof(double)); le = lt;"),
+    "direct_form_never_taken": ("if (cond < 0x1p-20) {", "if (cond < 0.0) {"),
     "reuse_prefix_dropped": ("orc_merge(s->ring_o + (ring_base + e) * d, s->ring_lse[ring_base + e], ot, lt, d, o, &l);",
                              "memcpy(o, ot, (size_t)d * sizeof(double)); l = lt;"),
 }
