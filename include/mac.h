@@ -264,7 +264,9 @@ mac_status mac_debug_read_ring(mac_handle h, int req, int32_t *host_pos, uint16_
  *                 ((b * kv_heads + g) * ctx_stride + j) * head_dim
  *                 (the contiguous layout of a mac_create handle with
  *                 page_size 0, ctx_stride = max_ctx rounded up to 16)
- *   host_lens     host int32 [batch], tokens of each request, 1..ctx_stride
+ *   host_lens     host int32 [batch], tokens of each request, 1..ctx_stride;
+ *                 slots past a request's length are never used, whatever
+ *                 they hold (NaN included)
  *   dev_q         bf16 [batch][heads][head_dim], post-RoPE query
  *   dev_out       bf16 [batch][heads][head_dim]; dev_lse fp32 [batch][heads]
  *                 natural-log LSE, or NULL
@@ -280,7 +282,9 @@ mac_status mac_debug_read_ring(mac_handle h, int req, int32_t *host_pos, uint16_
  * and overwrite it: calls whose GPU work can overlap (other streams, other
  * host threads) race and must be serialised by the caller.  Async on
  * stream; returns MAC_ERR_INVALID_ARG for bad arguments, MAC_ERR_CUDA if a
- * launch fails. */
+ * launch fails.  Every block index the kernels form is checked on the host
+ * first (lengths within ctx_stride), so this call has no device-side error
+ * to report and none is read back: MAC_OK means the work was launched. */
 mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, int head_dim, int64_t ctx_stride,
                                  const void *dev_k, const void *dev_v, const int32_t *host_lens,
                                  const void *dev_q, void *dev_out, float *dev_lse, float sm_scale,

@@ -519,10 +519,16 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             }
             const char *ksrc = reinterpret_cast<const char *>(L.k_pool + off) + src_off0;
             const char *vsrc = reinterpret_cast<const char *>(L.v_pool + off) + src_off0;
+            // value rows past the segment's end are staged as zeros: their
+            // weight is exactly 0, and 0 x (whatever the slot holds) must not
+            // turn into NaN (key rows there are masked by the score select)
+            const int vrows = shi - pg * 16;
 #pragma unroll
             for (int i = 0; i < CPT; i++) cp_async16(st + dst_off[i], ksrc + i * (GT / 16) * 256);
 #pragma unroll
-            for (int i = 0; i < CPT; i++) cp_async16(st + 4096 + dst_off[i], vsrc + i * (GT / 16) * 256);
+            for (int i = 0; i < CPT; i++)
+                cp_async16_zfill(st + 4096 + dst_off[i], vsrc + i * (GT / 16) * 256,
+                                 crow0 + i * (GT / 16) < vrows ? 16u : 0u);
         };
 
 #pragma unroll

@@ -65,6 +65,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte copy whose first src_bytes (0 or 16) come from src and the rest
+// are written as zeros; nothing is read from src when src_bytes is 0.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
 // Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
 {

@@ -14,9 +14,13 @@
 // library until the process exits (16 MiB each).  No call here allocates.
 //
 // The array is shared by every call on a device and keeps the previous
-// call's contents; each call rewrites all of it that it reads.  Calls whose
-// GPU work overlaps (different streams, or different host threads on one
-// device) race on it and must be serialised by the caller.
+// call's contents.  Where each region sits depends on the call's shape, so a
+// call finds another call's bytes under every region: it writes the plan
+// inputs, the page-pool claim counters and the stats / error words before
+// the attention kernel reads them, and the attention kernel writes the work
+// list and partials before Combine reads them.  Calls whose GPU work
+// overlaps (different streams, or different host threads on one device)
+// race on it and must be serialised by the caller.
 #include "../../include/mac.h"
 #include "mac_internal.cuh"
 
@@ -94,11 +98,14 @@ NoallocCarve carve(int batch, int heads, int kv_heads, int item_cap)
 }
 
 // One block: the span of every (request, KV head) group is [0, len); the
-// attention kernel plans its work items from these.
+// attention kernel plans its work items from these.  Each group's two
+// page-pool claim counters start at zero (the attention kernel takes pool
+// pages by atomicAdd on them).
 __global__ void noalloc_prepare_kernel(Layout L, NoallocPlanArgs p)
 {
     const int nbg = p.batch * p.kv_heads;
     for (int bg = threadIdx.x; bg < nbg; bg += blockDim.x) L.grp_lo[bg] = 0;
+    for (int i = threadIdx.x; i < 2 * nbg; i += blockDim.x) L.seg_claim[i] = 0;
     for (int i = threadIdx.x; i < p.batch * L.H; i += blockDim.x) L.dec_lo[i] = 0;
     for (int b = threadIdx.x; b < p.batch; b += blockDim.x) L.m_cur[b] = p.lens[b];
 }

@@ -316,3 +316,33 @@ def test_host_buffer_step_refuses_pageable_memory():
     assert st == -1
     torch.cuda.synchronize()
     assert p.mac.stats()["steps"] == 0
+
+
+@pytest.mark.parametrize("amend_band", [0, 1])
+def test_band_holding_the_mass_takes_the_direct_form(amend_band):
+    """Log-domain removal is ill-conditioned when the band [m-r+1, m] holds
+    almost all of AS_{1:m}'s mass.  Each step's new key is 4x the sum of its
+    KV group's post-RoPE queries (fresh random queries every step), so the
+    new token outscores every other by a wide margin and 1 - e^delta falls
+    far below 1/32: the GPU must then store AS_{1:m-r} in its direct form
+    (counted in removal_direct), on hit and on miss steps, and the ring
+    entries must still match the oracle's."""
+    c = cfg(steps=14, rho=0.995, ring_len=4, band_r=8, context=300)
+    p = _pair(c, amend_band=amend_band)
+    gen = torch.Generator().manual_seed(31)
+    B, H, Hkv, G, d = c.batch, c.heads, c.kv_heads, c.group, c.head_dim
+    for t in range(c.steps):
+        qp = W.to_bf16(torch.randn((B, H, d), generator=gen, dtype=torch.float64))
+        p.inputs["q_post"][t] = qp
+        p.inputs["k_new"][t] = W.to_bf16(4.0 * qp.double().reshape(B, Hkv, G, d).sum(2))
+    hits = misses = 0
+    for t in range(c.steps):
+        ref, _ = p.mac_step(t, force=True)
+        if c.context + t + 1 > c.band_r:
+            hits += int(ref["hit"].sum())
+            misses += int((~ref["hit"]).sum())
+    assert hits > 0 and misses > 0
+    st = p.mac.stats()
+    assert st["device_error"] == 0
+    # every (request, head) of every step past the band is ill-conditioned
+    assert st["removal_direct"] == c.steps * B * H, st["removal_direct"]

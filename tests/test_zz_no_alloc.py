@@ -5,9 +5,13 @@ runtime with one arena planned at start-up, a latency-critical loop that must
 not call cudaMalloc, a plug-in host that only hands over its buffers).  This
 entry point keeps its scratch in a fixed array inside the library instead of
 a caller-allocated buffer.  The test drives it through the C ABI and checks
-it against mac_full_step -- the handle-based entry point computing the same
-attention -- on two consecutive decode steps, with the tolerance the other
-GPU tests use, and checks that an oversized call is refused.
+every call against the fp64 oracle's full attention, element by element,
+with the tolerance the other GPU tests use, over consecutive calls of
+different shapes (the scratch regions move with the shape, so each call
+finds the previous call's bytes under its own), at contexts long enough for
+the attention kernel's shared page pools to engage, with every KV slot past
+a request's length holding NaN.  It also checks that an oversized call is
+refused.
 
 Kept in a file of its own that pytest collects last, so a stop-at-first-
 failure run has already run every other test when it gets here.
@@ -24,12 +28,6 @@ pytestmark = [pytest.mark.gpu,
 OUT_TOL, LSE_TOL = 5e-3, 1e-4
 
 
-def _rel_err(a, b):
-    a = a.float().cpu().numpy().astype(np.float64)
-    b = b.float().cpu().numpy().astype(np.float64)
-    return (np.abs(a - b).max(axis=-1) / np.maximum(np.abs(b).max(axis=-1), 1e-30)).max()
-
-
 def _noalloc(lib, B, H, Hkv, ctx_stride, K, V, lens, q, out, lse):
     lens_c = (ctypes.c_int32 * B)(*lens)
     return lib.mac_attention_noalloc(B, H, Hkv, 128, ctx_stride, ctypes.c_void_p(K.data_ptr()),
@@ -39,41 +37,63 @@ def _noalloc(lib, B, H, Hkv, ctx_stride, K, V, lens, q, out, lse):
                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def test_noalloc_matches_full_step_on_two_calls():
-    from kv_cache_computation_gb300 import MacAttention, build
+def _oracle_attention(K, V, lens, q_bits, H):
+    """AS_{1:len}(q) per request and query head from the fp64 oracle.
+    K, V uint16 [B, T, Hkv, d]; q_bits uint16 [B, H, d]."""
+    import oracle
+    B = K.shape[0]
+    st = oracle.MacState(K.copy(), V.copy(), H, 1, 1, 0.0)
+    idx = np.asarray(lens) - 1
+    for b in range(B):
+        st.reset(b, int(idx[b]))               # the last token is appended by the full step itself
+    k_last = np.ascontiguousarray(K[np.arange(B), idx])
+    v_last = np.ascontiguousarray(V[np.arange(B), idx])
+    return st.full_step(q_bits, k_last, v_last)
+
+
+def _call_case(lib, B, H, Hkv, lens, seed):
     from kv_cache_computation_gb300 import _native as N
     from kv_cache_computation_gb300 import workloads as W
+    T = max(lens)
+    ctx_stride = (T + 15) // 16 * 16 + 16
+    cfg = W.DecodeConfig(f"noalloc_{B}x{H}x{Hkv}", B, H, Hkv, 128, T, 1, 1, 1, 0.0, paged=False, seed=seed)
+    K, V = W.prefill_kv(cfg, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q = torch.randn((B, H, 128), generator=g, device="cuda").to(torch.bfloat16)
+    # the caller's cache: every slot NaN, then each request's tokens
+    Kc = torch.full((B, Hkv, ctx_stride, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    Vc = torch.full_like(Kc, float("nan"))
+    for b, n in enumerate(lens):
+        Kc[b, :, :n] = K[b, :n].transpose(0, 1)
+        Vc[b, :, :n] = V[b, :n].transpose(0, 1)
+    out = torch.empty((B, H, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    st = _noalloc(lib, B, H, Hkv, ctx_stride, Kc, Vc, lens, q, out, lse)
+    assert st == 0, N.STATUS.get(st, st)
+    torch.cuda.synchronize()
+    ref = _oracle_attention(W.bf16_bits(K), W.bf16_bits(V), lens, W.bf16_bits(q), H)
+    o = out.float().cpu().numpy().astype(np.float64)
+    err = np.abs(o - ref["out"]).max(-1) / np.maximum(np.abs(ref["out"]).max(-1), 1e-30)
+    assert np.isfinite(o).all(), "NaN from the slots past a request's length reached the output"
+    assert err.max() <= OUT_TOL, f"{B}x{H}x{Hkv}: output error {err.max():.3g}"
+    lerr = np.abs(lse.cpu().numpy().astype(np.float64) - ref["lse"]).max()
+    assert lerr <= LSE_TOL, f"{B}x{H}x{Hkv}: lse error {lerr:.3g}"
+
+
+def test_noalloc_matches_oracle_on_consecutive_calls_of_different_shapes():
+    from kv_cache_computation_gb300 import build
+    from kv_cache_computation_gb300 import _native as N
     build.build()
     lib = N.lib()
-    B, H, Hkv, ctx, steps = 2, 32, 8, 700, 2
-    cfg = W.DecodeConfig("noalloc_gqa32x8_ctx700_b2", B, H, Hkv, 128, ctx, steps, 4, 32, 0.3, paged=False)
-    K0, V0 = W.prefill_kv(cfg)
-    inp = W.decode_inputs(cfg)
-    max_ctx = ctx + steps
-    mac = MacAttention(H, Hkv, 128, 4, 32, 0.3, max_batch=B, max_ctx=max_ctx, page_size=0)
-    ctx_stride = (max_ctx + 15) // 16 * 16
-    # the caller's own KV cache in the same contiguous layout
-    Kc = torch.zeros((B, Hkv, ctx_stride, 128), dtype=torch.bfloat16, device="cuda")
-    Vc = torch.zeros_like(Kc)
-    for b in range(B):
-        mac.append_kv(b, K0[b].cuda().contiguous(), V0[b].cuda().contiguous())
-        Kc[b, :, :ctx] = K0[b].transpose(0, 1).cuda()
-        Vc[b, :, :ctx] = V0[b].transpose(0, 1).cuda()
-    for t in range(steps):                       # two calls in a row, state carried over
-        q = inp["q_post"][t].cuda().contiguous()
-        kn = inp["k_new"][t].cuda().contiguous()
-        vn = inp["v_new"][t].cuda().contiguous()
-        ref_out, ref_lse = mac.full_step(q, kn, vn)
-        Kc[:, :, ctx + t] = kn
-        Vc[:, :, ctx + t] = vn
-        out = torch.empty_like(ref_out)
-        lse = torch.empty_like(ref_lse)
-        st = _noalloc(lib, B, H, Hkv, ctx_stride, Kc, Vc, [ctx + t + 1] * B, q, out, lse)
-        assert st == 0, N.STATUS.get(st, st)
-        torch.cuda.synchronize()
-        assert _rel_err(out, ref_out) <= OUT_TOL
-        assert (lse - ref_lse).abs().max().item() <= LSE_TOL
-    mac.close()
+    # one request (8 groups, ~66-page work items), then eight ragged requests
+    # (64 groups, ~250-page items), a 4-group call with an 8-head group and a
+    # 45-token request, and the first shape again: every call's work items
+    # are long enough for the shared page pools, whose claim counters sit
+    # elsewhere in the array from one shape to the next
+    _call_case(lib, 1, 32, 8, [39997], seed=11)
+    _call_case(lib, 8, 32, 8, [20000 + 37 * b for b in range(8)], seed=12)
+    _call_case(lib, 2, 32, 4, [30001, 45], seed=13)
+    _call_case(lib, 1, 32, 8, [39997], seed=14)
 
 
 def test_noalloc_refuses_what_its_scratch_cannot_hold():
