@@ -123,23 +123,22 @@ KERNEL_SOURCES = [os.path.join(ROOT, "kv_cache_computation_gb300", "csrc", f)
                   for f in ("mac_attention.cu", "mac_device.cuh", "mac_internal.cuh")]
 
 
-def profiled_traffic(kernel_files):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
-    prof = os.path.join(ROOT, "profiles", "attention_kernel_128k.md")
-    if not os.path.exists(prof):
-        return None
-    sha = kernel_source_sha(kernel_files)
-    vals = {}
-    for ln in open(prof):
-        if ln.startswith("traffic_bytes_per_launch:") or ln.startswith("kernel_source_sha256_16:"):
-            k, v = ln.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != sha:
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_128k.json")
+
+
+def profiled_traffic(kernel_files, path=TRAFFIC_FILE):
+    """DRAM bytes per launch of the attention kernel (ncu dram__bytes_read.sum
+    + dram__bytes_write.sum) as recorded in the committed capture file, if
+    that capture was taken on the current kernel sources; else None."""
+    if not os.path.exists(path):
         return None
     try:
-        return float(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_sha256_16") != kernel_source_sha(kernel_files):
+            return None
+        return float(rec["traffic_bytes_per_launch"])
+    except (OSError, ValueError, KeyError, TypeError):
         return None
 
 
@@ -295,13 +294,134 @@ def cpu_model():
     return platform.processor() or platform.machine()
 
 
+def graph_time(fn, t0, n, stream, eager=False):
+    """us per call of fn(t0..t0+n-1): captured once into a CUDA graph and
+    replayed (per-call launches when eager), device events on ``stream``."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    g = None
+    if not eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for t in range(t0, t0 + n):
+                    fn(t)
+        torch.cuda.synchronize()
+    e0.record(stream)
+    if g is not None:
+        g.replay()
+    else:
+        for t in range(t0, t0 + n):
+            fn(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / n
+
+
+def attention_bytes(st, B, H, G):
+    """Algorithmic bytes of the attention launches counted in ``st``: 512 B
+    per streamed (KV head, token), 256 B of query per head and step, 520 B
+    of partial summary per work item and head."""
+    return st["kv_tokens_read"] * BYTES_PER_KV_TOKEN + st["steps"] * B * H * 256 + st["work_items"] * G * (128 * 4 + 8)
+
+
+def method_points(dev, peak, specs, steps=48, warm=4, prof_steps=16, eager=False, on_point=None):
+    """The MAC step against the in-build full split-KV step (mac_full_step)
+    on forced-hit workloads (one handle per (kv_heads, batch, context), the
+    same prefill and inputs for both): us/step, KV bytes read vs full, head
+    hit rate, and the HBM fraction of the step (KV bytes read / step time)
+    and of its attention kernel (algorithmic bytes / event-timed launch,
+    from a second pass with events between the kernels)."""
+    from kv_cache_computation_gb300 import MacAttention
+    from kv_cache_computation_gb300 import workloads as W
+    stream = torch.cuda.current_stream()
+    res = []
+    for kv, B, ctx, rates in specs:
+        n_all = warm + steps + prof_steps
+        base = W.sweep_point(ctx, B, 0.0, kv, steps=n_all)
+        H, G = base.heads, base.group
+        max_ctx = ctx + n_all + 2
+        mac = MacAttention(H, kv, 128, base.ring_len, base.band_r, base.tau, max_batch=B, max_ctx=max_ctx,
+                           page_size=16)
+        pt = W.page_tables(B, (max_ctx + 15) // 16, seed=base.seed).to(dev)
+        for b in range(B):
+            mac.set_page_table(b, pt[b].contiguous())
+        Kp, Vp = W.prefill_kv(base, device=dev)
+        out = torch.empty((B, H, 128), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+
+        def restart():
+            mac.sync()
+            for b in range(B):
+                mac.reset_request(b)
+                mac.append_kv(b, Kp[b], Vp[b])
+            torch.cuda.synchronize()
+
+        def measure(step, t_warm):
+            for t in range(t_warm):
+                step(t)
+            mac.sync()
+            mac.reset_stats()
+            us = graph_time(step, t_warm, steps, stream, eager=eager)
+            mac.join()
+            st = mac.stats()
+            mac.reset_stats()
+            mac.set_profiling(True)
+            for t in range(t_warm + steps, t_warm + steps + prof_steps):
+                step(t)
+            mac.join()
+            torch.cuda.synchronize()
+            pr = mac.profile()
+            st_p = mac.stats()
+            mac.set_profiling(False)
+            n_p = max(1, pr["steps"])
+            attn_us = pr["attention_ms"] * 1e3 / n_p
+            attn_gbs = attention_bytes(st_p, B, H, G) / n_p / (attn_us * 1e-6) / 1e9
+            kv_read, kv_full = _kv_bytes(st)
+            phases = {k.replace("_ms", ""): round(pr[k] * 1e3 / n_p, 2)
+                      for k in ("match_plan_ms", "attention_ms", "combine_ms")}
+            phases["work_items"] = round(st_p["work_items"] / n_p, 1)
+            return us, st, kv_read, kv_full, attn_us, attn_gbs, phases
+
+        for rate in rates:
+            cfg = W.sweep_point(ctx, B, rate, kv, steps=n_all)
+            inp = W.decode_inputs(cfg, device=dev)
+            restart()
+            us, st, kv_read, kv_full, attn_us, attn_gbs, ph = measure(
+                lambda t: mac.decode_step(inp["q_pre"][t], inp["q_post"][t], inp["k_new"][t], inp["v_new"][t],
+                                          out=out, lse=lse), warm)
+            restart()
+            f_us, _, f_read, _, f_attn_us, f_attn_gbs, f_ph = measure(
+                lambda t: mac.full_step(inp["q_post"][t], inp["k_new"][t], inp["v_new"][t], out=out, lse=lse), warm)
+            step_gbs = kv_read / steps / (us * 1e-6) / 1e9
+            f_step_gbs = f_read / steps / (f_us * 1e-6) / 1e9
+            res.append({"kind": "mqa" if kv == 1 else "gqa", "heads": H, "kv_heads": kv, "batch": B, "context": ctx,
+                        "forced_hit": rate, "mac_us_per_step": round(us, 2), "full_us_per_step": round(f_us, 2),
+                        "ratio_full_over_mac": round(f_us / us, 3),
+                        "kv_bytes_read_vs_full": round(kv_read / max(1, kv_full), 4),
+                        "hit_rate": round(st["hits"] / max(1, st["head_decisions"]), 4),
+                        "mac_step_hbm_frac": round(step_gbs / peak, 4),
+                        "full_step_hbm_frac": round(f_step_gbs / peak, 4),
+                        "mac_attention_us": round(attn_us, 2), "mac_attention_frac": round(attn_gbs / peak, 4),
+                        "full_attention_us": round(f_attn_us, 2), "full_attention_frac": round(f_attn_gbs / peak, 4),
+                        "mac_phase_us": ph, "full_phase_us": f_ph})
+            if on_point is not None:
+                on_point(res[-1])
+        del Kp, Vp
+        mac.close()
+        torch.cuda.empty_cache()
+    return res
+
+
 def bench_ours(args, ws, rank, local):
     from kv_cache_computation_gb300 import MacAttention
     from kv_cache_computation_gb300 import workloads as W
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K_steps, W_steps = args.steps, args.warmup
-    total_steps = W_steps + 5 * K_steps + 2
+    total_steps = W_steps + 6 * K_steps + 2
     cfg = workload(args.workload, args.band_r, total_steps)
     B, H, Hkv, G = cfg.batch, cfg.heads, cfg.kv_heads, cfg.group
 
@@ -504,6 +624,14 @@ def bench_ours(args, ws, rank, local):
     if not all(torch.isfinite(x.float()).all() for x in (h_out[-1], h_lse[-1])):
         raise RuntimeError("host-buffer decode step left non-finite results")
 
+    # the build's own full split-KV decode (every head a miss, no ring) on
+    # the same handle and inputs, timed like the headline
+    f_first = h_first + K_steps
+    mac.sync()
+    full_us = max_over_ranks(graph_time(lambda t: mac.full_step(inp["q_post"][t], inp["k_new"][t], inp["v_new"][t],
+                                                                 out=out, lse=lse),
+                                        f_first, K_steps, stream, eager=args.eager), ws, dev)
+
     # bytes
     kv_read = st["kv_tokens_read"] * BYTES_PER_KV_TOKEN
     kv_full = st["kv_tokens_full"] * BYTES_PER_KV_TOKEN
@@ -544,7 +672,9 @@ def bench_ours(args, ws, rank, local):
         "kv_bytes_read_vs_full": round(kv_read / kv_full, 5) if kv_full else None,
         "hit_rate": round(st["hits"] / max(1, st["head_decisions"]), 5),
         "phase_us_per_step": {k.replace("_ms", ""): round(v * 1e3 / launches, 3) for k, v in prof.items()
-                              if k.endswith("_ms")},
+                              if k.endswith("_ms") and (k != "amend_ms" or args.amend_band == 1)},
+        "full_us_per_step": round(full_us, 3),
+        "ratio_full_over_mac": round(full_us / us_step, 4),
         "roofline": {"kernel": "attention_kernel", "bound": "hbm",
                      "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4) if achieved else None,
@@ -554,7 +684,10 @@ def bench_ours(args, ws, rank, local):
                      "avg_launch_us": round(attn_s / launches * 1e6, 3),
                      "timing": "CUDA events around each attention launch over a second pass of K steps "
                                "(events between kernels disable launch overlap, so that pass is not the headline)",
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     "traffic_source": ("quoted from profiles/attention_kernel_128k.json: one ncu capture of this "
+                                        "kernel source on this workload (hash-checked)") if traffic else
+                                       "no ncu capture of the current kernel source"},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
                 "api": "mac_decode_step_host: pinned host inputs read and results written in place by the "
@@ -569,6 +702,14 @@ def bench_ours(args, ws, rank, local):
                   "work_items_per_step": round(items / max(1, steps), 1)},
     }
     mac.sync()
+    if not args.no_method_points:
+        # the method against full attention where hits skip KV: GQA 1 x 128K
+        # at 90 % forced hits, MQA 1 x 128K and 32 x 128K at 0 and 90 %
+        specs = [(8, 1, 131072, (0.9,)), (1, 1, 131072, (0.0, 0.9)), (1, 32, 131072, (0.0, 0.9))]
+        result["method_points"] = {
+            "workload": "forced-hit streams (per request, KV group and step), paged 16, ring 16, r 64, tau 0.3; "
+                        "us/step from CUDA-graph replays of 48 steps; fractions of the measured HBM peak",
+            "points": method_points(dev, peak, specs)}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         us, cores, sample, extra = run_oracle(cfg, Kp, Vp, inp, args.cpu_budget, max_steps=min(K_steps, 256))
         result["cpu_baseline"] = {"value": round(us, 1), "unit": "us/step", "cores": cores, "kind": "oracle",
@@ -690,95 +831,21 @@ def bench_sweep(args, ws, rank, local):
     """Context x batch x forced hit rate, MQA and GQA: the MAC path against the
     build's own full split-KV decode (mac_full_step) on the same handle.
     Prints one JSON line per point (rank 0)."""
-    from kv_cache_computation_gb300 import MacAttention
-    from kv_cache_computation_gb300 import workloads as W
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    steps, warm = args.steps, args.warmup
-    stream = torch.cuda.current_stream()
     ctxs = [int(x) for x in args.sweep_contexts.split(",")]
     batches = [int(x) for x in args.sweep_batches.split(",")]
-    rates = [float(x) for x in args.sweep_rates.split(",")]
+    rates = tuple(float(x) for x in args.sweep_rates.split(","))
     kvs = [int(x) for x in args.sweep_kv_heads.split(",")]
+    peak, _ = measured_peaks()
+    specs = [(kv, B, ctx, rates) for kv in kvs for ctx in ctxs for B in batches]
 
-    def timed(fn, t0, n):
-        """us per step of fn(t0..t0+n-1): captured into a CUDA graph and
-        replayed (per-call launches with --eager)."""
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        g = None
-        if not args.eager:
-            cap = torch.cuda.Stream()
-            cap.wait_stream(stream)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(cap):
-                with torch.cuda.graph(g, stream=cap):
-                    for t in range(t0, t0 + n):
-                        fn(t)
-            torch.cuda.synchronize()
-        e0.record(stream)
-        if g is not None:
-            g.replay()
-        else:
-            for t in range(t0, t0 + n):
-                fn(t)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / n
+    def emit(pt):
+        if rank == 0:
+            print(json.dumps({"workload": "forced_hit_sweep", **pt}), flush=True)
 
-    for kv in kvs:
-        for ctx in ctxs:
-            for B in batches:
-                base = W.sweep_point(ctx, B, 0.0, kv, steps=steps + 1)
-                H = base.heads
-                max_ctx = ctx + steps + 2
-                mac = MacAttention(H, kv, 128, base.ring_len, base.band_r, base.tau, max_batch=B, max_ctx=max_ctx,
-                                   page_size=16)
-                pt = W.page_tables(B, (max_ctx + 15) // 16, seed=base.seed).to(dev)
-                for b in range(B):
-                    mac.set_page_table(b, pt[b].contiguous())
-                Kp, Vp = W.prefill_kv(base, device=dev)
-                out = torch.empty((B, H, 128), dtype=torch.bfloat16, device=dev)
-                lse = torch.empty((B, H), dtype=torch.float32, device=dev)
-
-                def restart():
-                    mac.sync()
-                    for b in range(B):
-                        mac.reset_request(b)
-                        mac.append_kv(b, Kp[b], Vp[b])
-                    torch.cuda.synchronize()
-
-                restart()
-                inp0 = W.decode_inputs(base, device=dev)
-                full_us = timed(lambda t: mac.full_step(inp0["q_post"][t], inp0["k_new"][t], inp0["v_new"][t],
-                                                        out=out, lse=lse), 0, steps)
-                for rate in rates:
-                    cfg = W.sweep_point(ctx, B, rate, kv, steps=steps + 1)
-                    inp = W.decode_inputs(cfg, device=dev)
-                    restart()
-                    step = lambda t: mac.decode_step(inp["q_pre"][t], inp["q_post"][t], inp["k_new"][t],
-                                                     inp["v_new"][t], out=out, lse=lse)
-                    for t in range(warm):
-                        step(t)
-                    mac.sync()
-                    mac.reset_stats()
-                    mac_us = timed(step, warm, steps - warm)
-                    mac.join()
-                    st = mac.stats()
-                    kv_read, kv_full = _kv_bytes(st)
-                    line = {"workload": "forced_hit_sweep", "kind": "mqa" if kv == 1 else "gqa", "heads": H,
-                            "kv_heads": kv, "context": ctx, "batch": B, "forced_hit": rate,
-                            "mac_us_step": round(mac_us, 2), "full_us_step": round(full_us, 2),
-                            "speedup_vs_full": round(full_us / mac_us, 3),
-                            "kv_bytes_read_vs_full": round(kv_read / max(1, kv_full), 4),
-                            "head_hit_rate": round(st["hits"] / max(1, st["head_decisions"]), 4),
-                            "mac_kv_gbs": round(kv_read / (steps - warm) / (mac_us * 1e-6) / 1e9, 1),
-                            "full_kv_gbs": round(kv_full / (steps - warm) / (full_us * 1e-6) / 1e9, 1)}
-                    if rank == 0:
-                        print(json.dumps(line), flush=True)
-                del Kp, Vp
-                mac.close()
-                torch.cuda.empty_cache()
+    method_points(dev, peak, specs, steps=args.steps, warm=args.warmup, prof_steps=min(16, args.steps),
+                  eager=args.eager, on_point=emit)
     return None
 
 
@@ -919,6 +986,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-method-points", action="store_true",
+                    help="skip the MAC-vs-full forced-hit points of the default run")
     ap.add_argument("--eager", action="store_true", help="time per-call launches instead of a CUDA-graph replay")
     ap.add_argument("--tau", type=float, default=None, help="threshold for the layer-stack workload (0.3 or 0.45)")
     ap.add_argument("--layers", type=int, default=48, help="layers of the stack workload")

@@ -115,7 +115,8 @@ typedef struct {
                               /* attention kernel                               */
     double combine_ms;        /* log-domain merge kernel (with Amend's removal  */
                               /* and ring insert when amend_band is 0)          */
-    double amend_ms;          /* Amend kernel (side stream, amend_band 1)       */
+    double amend_ms;          /* Amend kernel (side stream, amend_band 1); 0    */
+                              /* when Amend runs inside the merge kernel        */
     uint64_t steps;           /* steps timed                                    */
 } mac_profile;
 

@@ -149,6 +149,7 @@ struct mac_ctx {
     // combine end, amend start, amend end)
     bool prof = false;
     std::vector<cudaEvent_t> prof_ev;
+    std::vector<char> prof_amend;   // per profiled step: the side-stream Amend ran (its two events are set)
     size_t prof_steps = 0;
     double prof_acc[4] = {0, 0, 0, 0};
     uint64_t prof_done = 0;
@@ -248,11 +249,13 @@ mac_status prof_collect(mac_ctx *h)
         cudaEvent_t *e = &h->prof_ev[s * 6];
         float t[4] = {0, 0, 0, 0};
         MAC_CUDA(h, cudaEventSynchronize(e[3]));
-        MAC_CUDA(h, cudaEventSynchronize(e[5]));
         MAC_CUDA(h, cudaEventElapsedTime(&t[0], e[0], e[1]));
         MAC_CUDA(h, cudaEventElapsedTime(&t[1], e[1], e[2]));
         MAC_CUDA(h, cudaEventElapsedTime(&t[2], e[2], e[3]));
-        MAC_CUDA(h, cudaEventElapsedTime(&t[3], e[4], e[5]));
+        if (h->prof_amend[s]) {   // otherwise Amend ran inside Combine (or the step had none): 0
+            MAC_CUDA(h, cudaEventSynchronize(e[5]));
+            MAC_CUDA(h, cudaEventElapsedTime(&t[3], e[4], e[5]));
+        }
         for (int i = 0; i < 4; i++) h->prof_acc[i] += t[i];
         h->prof_done++;
     }
@@ -294,7 +297,10 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
     h->force_next = false;
 
     cudaEvent_t *pe = nullptr;
-    if (h->prof && h->prof_steps < kProfCap) pe = &h->prof_ev[h->prof_steps++ * 6];
+    if (h->prof && h->prof_steps < kProfCap) {
+        h->prof_amend[h->prof_steps] = (!full && h->cfg.amend_band == 1) ? 1 : 0;
+        pe = &h->prof_ev[h->prof_steps++ * 6];
+    }
     // Programmatic dependent launch overlaps each launch with its
     // predecessor's tail; event records between the kernels (profiling)
     // would sit between them, so it is used only when not profiling.
@@ -332,11 +338,6 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
         unsigned long long id = 0;
         MAC_CUDA(h, cudaStreamGetCaptureInfo(h->side, &cs, &id));
         h->amend_capture_id = cs == cudaStreamCaptureStatusActive ? id : 0;
-    } else if (pe) {
-        // Amend ran in the combine epilogue (or a full step has none): an
-        // empty interval on the main stream
-        MAC_CUDA(h, cudaEventRecord(pe[4], s));
-        MAC_CUDA(h, cudaEventRecord(pe[5], s));
     }
     for (int b = 0; b < batch; b++) {
         h->kv_len[b] += 1;
@@ -713,6 +714,7 @@ mac_status mac_set_profiling(mac_handle h, int enable)
     if (st != MAC_OK) return st;
     if (enable && h->prof_ev.empty()) {
         h->prof_ev.resize(kProfCap * 6, nullptr);
+        h->prof_amend.assign(kProfCap, 0);
         for (auto &e : h->prof_ev) MAC_CUDA(h, cudaEventCreate(&e));
     }
     MAC_CUDA(h, cudaDeviceSynchronize());

@@ -293,9 +293,17 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
 // Copy addressing: thread t of a lane group copies the 16-byte chunks
 // t + i * 32 NH of a page; its chunk column is fixed (t mod 16) and its rows
 // step by 2 NH, so every offset is a per-thread constant computed once.
+//
+// Groups of 16 or 32 heads (HM = true) put the heads on the M axis instead:
+// a warp owns a 16-head tile, so a page is read from shared memory by G / 16
+// warps rather than G / 8, and the score fragments are already the A
+// operand of P V (no transpose):
+//   S[16 heads x 16 tok] = Q[16 x 128] K^T[128 x 16]     2 x 8 mma
+//   O[16 heads x 128]   += P[16 x 16] V[16 x 128]        16 x 2 mma (hi + lo)
+// with Q in registers as A fragments and K, V read by ldmatrix as B.
 // ---------------------------------------------------------------------------
-template <int NW, int S, int NH>
-__global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a)
+template <int NW, int S, int NH, bool HM>
+__global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : MAC_HM_MIN_CTAS_32) : 1) attention_kernel(Layout L, StepArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int NP = NW / NH;
@@ -325,11 +333,28 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // K tile row (token) this lane addresses
     const int vtok = (lane & 7) + 8 * (lane >> 4);         // V tile row (token) this lane addresses
 
-    // Q^T fragments of group bg (head column 8 ht + r4) and the band+tail
-    // starts dec_lo of this thread's two head columns (8 ht + 2 c4, + 1).
-    auto load_group = [&](int bg, uint32_t (&qf)[8][2], int &d0, int &d1) {
+    // Query fragments of group bg and the band+tail starts dec_lo of this
+    // thread's two heads: Q^T as B (head column 8 ht + r4; heads 8 ht + 2 c4,
+    // + 1), or, with HM, Q as A (head rows 16 ht + r4, + 8: the two heads).
+    using QFrag = uint32_t[8][HM ? 4 : 2];
+    auto load_group = [&](int bg, QFrag &qf, int &d0, int &d1) {
         const int b = bg / L.Hkv, g = bg - b * L.Hkv;
         const size_t hrow = (size_t)b * L.H + (size_t)g * G;
+        if constexpr (HM) {
+            const int ha = 16 * ht + r4;
+            const uint32_t *qa = reinterpret_cast<const uint32_t *>(a.q_post + (hrow + ha) * kD);
+            const uint32_t *qb = reinterpret_cast<const uint32_t *>(a.q_post + (hrow + ha + 8) * kD);
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {
+                qf[kk][0] = qa[8 * kk + c4];
+                qf[kk][1] = qb[8 * kk + c4];
+                qf[kk][2] = qa[8 * kk + 4 + c4];
+                qf[kk][3] = qb[8 * kk + 4 + c4];
+            }
+            d0 = L.dec_lo[hrow + ha];
+            d1 = L.dec_lo[hrow + ha + 8];
+            return;
+        }
         const int hn = 8 * ht + r4;
         if (hn < G) {
             const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.q_post + (hrow + hn) * kD);
@@ -377,7 +402,7 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
     }
     pdl_wait();   // spans come from match_plan
     // the likely first item's queries load while the plan is made
-    uint32_t q_spec[8][2];
+    QFrag q_spec;
     int d0_spec = 0, d1_spec = 0;
     if (spec_bg >= 0) load_group(spec_bg, q_spec, d0_spec, d1_spec);
     cta_plan(L, a, ps);
@@ -402,21 +427,20 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         const int bg = item.x, ilo = item.y, ihi = item.z;
         const int b = bg / L.Hkv, g = bg - b * L.Hkv;
 
-        // Q^T fragments for head column n = r4 of this tile
-        uint32_t qf[8][2];
+        // query fragments of this warp's head tile
+        QFrag qf;
         int d0, d1;
         if (it == (int)blockIdx.x && bg == spec_bg) {
 #pragma unroll
-            for (int kk = 0; kk < 8; kk++) {
-                qf[kk][0] = q_spec[kk][0];
-                qf[kk][1] = q_spec[kk][1];
-            }
+            for (int kk = 0; kk < 8; kk++)
+#pragma unroll
+                for (int j = 0; j < (HM ? 4 : 2); j++) qf[kk][j] = q_spec[kk][j];
             d0 = d0_spec;
             d1 = d1_spec;
         } else {
             load_group(bg, qf, d0, d1);
         }
-        if constexpr (kAttnCudaCore) {   // the item's query rows (bf16), 8 per head tile, zeros past G
+        if constexpr (kAttnCudaCore && !HM) {   // the item's query rows (bf16), 8 per head tile, zeros past G
             __syncthreads();
             for (int i = threadIdx.x; i < NH * 8 * 16; i += NW * 32) {
                 const int hh = i >> 4, ch = i & 15;
@@ -431,17 +455,19 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         // computed here (see the pool below), so masks use its bounds
         const int glo = ps.lo[bg], ghi = ps.hi[bg], gsp = plan_split(L, a, glo, ghi);
         const int slo = item.w ? gsp : glo, shi = item.w ? ghi : gsp;
-        // this thread's two head columns and their first valid token (columns
-        // past the group's heads are computed and discarded: no mask)
-        const int hc0 = 8 * ht + 2 * c4, hc1 = hc0 + 1;
+        // this thread's two heads (columns, or rows with HM) and their first
+        // valid token (columns past the group's heads are computed and
+        // discarded: no mask)
+        const int hc0 = HM ? 16 * ht + r4 : 8 * ht + 2 * c4, hc1 = HM ? hc0 + 8 : hc0 + 1;
         const int lo0 = max(slo, d0);
         const int lo1 = max(slo, d1);
         const int lo_max = max(lo0, lo1);
 
         float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
-        float acc[8][4];
+        constexpr int NACC = HM ? 16 : 8;   // O^T m-tiles of 16 dims, or O n-tiles of 8 dims (HM)
+        float acc[NACC][4];
 #pragma unroll
-        for (int i = 0; i < 8; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        for (int i = 0; i < NACC; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
         const int pg0 = ilo >> 4, pg1 = (ihi - 1) >> 4;
         const int npg = pg1 - pg0 + 1;
@@ -581,6 +607,101 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             const uint32_t Vs = Ks + 4096;
             const int pg = k < npl ? pg0 + pl + k * NP : s_pool[pl][(k - npl) & 7];
 
+            if constexpr (HM) {
+                // S = Q K^T: n-tile j holds tokens 8 j .. 8 j + 7; this thread
+                // has head rows r4 (sc[j][0..1]) and r4 + 8 (sc[j][2..3]) at
+                // tokens 8 j + 2 c4, + 1
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                {
+                    const uint32_t kbase = Ks + vtok * 256;
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++) {
+                        const int ch = 2 * kk + ((lane >> 3) & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(b0, b1, b2, b3, kbase + ((ch ^ (vtok & 7)) << 4));
+                        mma_bf16(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+                        mma_bf16(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+                    }
+                }
+                float z[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; j++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) z[j][e] = sc[j][e] * sl2;
+                if (pg * 16 < lo_max || pg * 16 + 16 > shi) {
+#pragma unroll
+                    for (int j = 0; j < 2; j++)
+#pragma unroll
+                        for (int e = 0; e < 2; e++) {
+                            const int tok = pg * 16 + 8 * j + 2 * c4 + e;
+                            if (!(tok >= lo0 && tok < shi)) z[j][e] = -CUDART_INF_F;
+                            if (!(tok >= lo1 && tok < shi)) z[j][2 + e] = -CUDART_INF_F;
+                        }
+                }
+                float mx0 = fmaxf(fmaxf(z[0][0], z[0][1]), fmaxf(z[1][0], z[1][1]));
+                float mx1 = fmaxf(fmaxf(z[0][2], z[0][3]), fmaxf(z[1][2], z[1][3]));
+#pragma unroll
+                for (int o = 1; o < 4; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float bs0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+                const float bs1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+                float pr[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; j++) {
+                    pr[j][0] = exp2f(z[j][0] - bs0);
+                    pr[j][1] = exp2f(z[j][1] - bs0);
+                    pr[j][2] = exp2f(z[j][2] - bs1);
+                    pr[j][3] = exp2f(z[j][3] - bs1);
+                }
+                if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+                    const float al0 = exp2f(m0 - bs0), al1 = exp2f(m1 - bs1);
+                    l0 *= al0;
+                    l1 *= al1;
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        acc[i][0] *= al0;
+                        acc[i][1] *= al0;
+                        acc[i][2] *= al1;
+                        acc[i][3] *= al1;
+                    }
+                }
+                l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+                l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+                m0 = mn0;
+                m1 = mn1;
+                // P as the A operand (k = token): a0 rows r4 tokens 2 c4.., a1
+                // row r4 + 8, a2 / a3 the same at tokens 8 + 2 c4..; hi + lo
+                uint32_t ph[4], plo[4];
+#pragma unroll
+                for (int j = 0; j < 2; j++)
+#pragma unroll
+                    for (int rr = 0; rr < 2; rr++) {
+                        const __nv_bfloat162 hv = __floats2bfloat162_rn(pr[j][2 * rr], pr[j][2 * rr + 1]);
+                        const float2 fv = __bfloat1622float2(hv);
+                        const __nv_bfloat162 lv =
+                            __floats2bfloat162_rn(pr[j][2 * rr] - fv.x, pr[j][2 * rr + 1] - fv.y);
+                        ph[2 * j + rr] = bf16x2_bits(hv);
+                        plo[2 * j + rr] = bf16x2_bits(lv);
+                    }
+                // O += P V: ldmatrix.trans gives the B fragments of dim
+                // n-tiles 2 np and 2 np + 1
+                const uint32_t vbase = Vs + krow * 256;
+#pragma unroll
+                for (int np = 0; np < 8; np++) {
+                    const int ch = 2 * np + (lane >> 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(b0, b1, b2, b3, vbase + ((ch ^ (krow & 7)) << 4));
+                    mma_bf16(acc[2 * np], ph[0], ph[1], ph[2], ph[3], b0, b1);
+                    mma_bf16(acc[2 * np], plo[0], plo[1], plo[2], plo[3], b0, b1);
+                    mma_bf16(acc[2 * np + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+                    mma_bf16(acc[2 * np + 1], plo[0], plo[1], plo[2], plo[3], b2, b3);
+                }
+                continue;
+            }
+
             // S^T = K Q^T
             float s[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (kAttnCudaCore) {
@@ -690,14 +811,35 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         cp_async_wait<0>();
         __syncthreads();   // every page lane drained: stage memory is free
 
-        // sum l over the 8 lanes that share a head column
+        // sum l over the lanes that share a head: the 8 of a column, or (HM)
+        // the 4 of a row
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
+        for (int o = HM ? 1 : 4; o < (HM ? 4 : 32); o <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, o);
             l1 += __shfl_xor_sync(0xffffffffu, l1, o);
         }
+        // HM: this thread's fragment of head row h (acc[i][2 half], + 1: dims
+        // 8 i + 2 c4, + 1) into a [G][D] array, and the row's (max, sum)
+        auto store_rows = [&](float *o_base, float2 *ml_base, bool zero_empty) {
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                const int h = half ? hc1 : hc0;
+                const float mh = half ? m1 : m0, lh = half ? l1 : l0;
+                const bool none = zero_empty && mh == -CUDART_INF_F;
+                float *orow = o_base + (size_t)h * kD + 2 * c4;
+#pragma unroll
+                for (int i = 0; i < NACC; i++)
+                    *reinterpret_cast<float2 *>(orow + 8 * i) =
+                        none ? make_float2(0.f, 0.f) : make_float2(acc[i][2 * half], acc[i][2 * half + 1]);
+                if (c4 == 0) ml_base[h] = make_float2(mh, none ? 0.f : lh);
+            }
+        };
         if constexpr (NP == 1) {   // one page lane: the fragments are the item's partial
             const float NEG = -CUDART_INF_F;
+            if constexpr (HM) {
+                store_rows(L.part_o + (size_t)it * G * kD, L.part_ml + (size_t)it * G, true);
+                continue;
+            }
             if (hc0 < G) {
                 float *o0 = L.part_o + ((size_t)it * G + hc0) * kD;
                 const bool none = m0 == NEG;
@@ -723,7 +865,9 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
         // stage each page lane's partial in shared memory, then merge lanes
         float *red_o = reinterpret_cast<float *>(smem);                               // [NP][G][D]
         float2 *red_ml = reinterpret_cast<float2 *>(red_o + (size_t)NP * G * kD);     // [NP][G]
-        if (hc0 < G) {
+        if constexpr (HM) {
+            store_rows(red_o + (size_t)pl * G * kD, red_ml + pl * G, false);
+        } else if (hc0 < G) {
             float *o0 = red_o + ((size_t)pl * G + hc0) * kD;
 #pragma unroll
             for (int i = 0; i < 8; i++) {
@@ -732,7 +876,7 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
             }
             if (r4 == 0) red_ml[pl * G + hc0] = make_float2(m0, l0);
         }
-        if (hc1 < G) {
+        if (!HM && hc1 < G) {
             float *o1 = red_o + ((size_t)pl * G + hc1) * kD;
 #pragma unroll
             for (int i = 0; i < 8; i++) {
@@ -769,7 +913,10 @@ __global__ void __launch_bounds__(NW * 32) attention_kernel(Layout L, StepArgs a
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-static int head_tiles(int G) { return (G + 7) / 8; }
+// Groups of 16 or 32 heads put the heads on the mma M axis (16-head tiles);
+// smaller groups put them on N (8-head tiles).
+static bool heads_on_m(int G) { return kHeadsOnM && !kAttnCudaCore && G % 16 == 0; }
+static int head_tiles(int G) { return heads_on_m(G) ? G / 16 : (G + 7) / 8; }
 
 static size_t attention_smem(int G)
 {
@@ -780,10 +927,10 @@ static size_t attention_smem(int G)
     return (pipe > red ? pipe : red) + q_tiles;
 }
 
-template <int NH>
+template <int NH, bool HM>
 static cudaError_t attention_config_nh(size_t smem, int *ctas_per_sm)
 {
-    auto k = attention_kernel<kAttnWarps, kAttnStages, NH>;
+    auto k = attention_kernel<kAttnWarps, kAttnStages, NH, HM>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, k, kAttnWarps * 32, smem);
@@ -792,22 +939,27 @@ static cudaError_t attention_config_nh(size_t smem, int *ctas_per_sm)
 cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm)
 {
     *smem = attention_smem(G);
+    if (heads_on_m(G)) return G == 16 ? attention_config_nh<1, true>(*smem, ctas_per_sm)
+                                      : attention_config_nh<2, true>(*smem, ctas_per_sm);
     switch (head_tiles(G)) {
-    case 1: return attention_config_nh<1>(*smem, ctas_per_sm);
-    case 2: return attention_config_nh<2>(*smem, ctas_per_sm);
-    default: return attention_config_nh<4>(*smem, ctas_per_sm);
+    case 1: return attention_config_nh<1, false>(*smem, ctas_per_sm);
+    case 2: return attention_config_nh<2, false>(*smem, ctas_per_sm);
+    default: return attention_config_nh<4, false>(*smem, ctas_per_sm);
     }
 }
-
-
 
 cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)
 {
     const dim3 grid(a.grid_ctas), block(kAttnWarps * 32);
+    if (heads_on_m(L.G)) {
+        if (L.G == 16)
+            return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1, true>, grid, block, smem, s, a.pdl, L, a);
+        return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2, true>, grid, block, smem, s, a.pdl, L, a);
+    }
     switch (head_tiles(L.G)) {
-    case 1: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1>, grid, block, smem, s, a.pdl, L, a);
-    case 2: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2>, grid, block, smem, s, a.pdl, L, a);
-    default: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 4>, grid, block, smem, s, a.pdl, L, a);
+    case 1: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1, false>, grid, block, smem, s, a.pdl, L, a);
+    case 2: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2, false>, grid, block, smem, s, a.pdl, L, a);
+    default: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 4, false>, grid, block, smem, s, a.pdl, L, a);
     }
 }
 

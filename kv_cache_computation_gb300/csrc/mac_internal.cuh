@@ -55,6 +55,21 @@ constexpr int kDynMinPages = 32;
 // fp32 FMA instead of mma.sync (same tiles, same layouts, q staged in shared
 // memory); selected at compile time, never at run time.
 constexpr bool kAttnCudaCore = MAC_ATTN_CUDA_CORE != 0;
+#ifndef MAC_ATTN_HEADS_ON_M
+#define MAC_ATTN_HEADS_ON_M 1
+#endif
+// Groups of 16 and 32 heads take the heads-on-M attention tiles (0: the
+// 8-head N tiles of smaller groups for every group size; comparison build).
+constexpr bool kHeadsOnM = MAC_ATTN_HEADS_ON_M != 0;
+// Resident CTAs per SM the heads-on-M kernel is register-budgeted for: 2 for
+// 16-head groups (one 16-head tile per warp, 4 page lanes), 3 for 32-head
+// groups (2 tiles, 2 page lanes; ~170 registers, a few bytes spilled).
+#ifndef MAC_HM_MIN_CTAS_16
+#define MAC_HM_MIN_CTAS_16 2
+#endif
+#ifndef MAC_HM_MIN_CTAS_32
+#define MAC_HM_MIN_CTAS_32 3
+#endif
 constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
 constexpr int kMinChunk = 64;           // smallest work-item span in tokens
 constexpr int kPlanCache = 1024;        // groups the planner caches in shared memory

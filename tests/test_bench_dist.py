@@ -1,6 +1,7 @@
 """The benchmark's multi-process path on CPU (gloo, world size 2): every rank
 runs its own replica (the decode path has no exchange step), the timing is the
 maximum over ranks and counts are summed; rank 0 alone prints."""
+import json
 import os
 import socket
 import sys
@@ -84,3 +85,9 @@ def test_launch_count_and_traffic_provenance(tmp_path):
     src.write_text("kernel v2")
     assert bench.kernel_source_sha([str(src)]) != h1 and len(h1) == 16
     assert any(f.endswith("mac_attention.cu") for f in bench.KERNEL_SOURCES)
+    rec = tmp_path / "cap.json"
+    rec.write_text(json.dumps({"kernel_source_sha256_16": h1, "traffic_bytes_per_launch": 123.0}))
+    assert bench.profiled_traffic([str(src)], str(rec)) is None      # sources changed since the capture
+    src.write_text("kernel v1")
+    assert bench.profiled_traffic([str(src)], str(rec)) == 123.0
+    assert bench.profiled_traffic([str(src)], str(tmp_path / "absent.json")) is None
