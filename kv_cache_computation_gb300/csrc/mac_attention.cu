@@ -14,15 +14,22 @@ namespace {
 // ---------------------------------------------------------------------------
 // Planning (prologue of every attention CTA; all CTAs derive the same plan).
 // Per (request, kv-head) group the streamed span is [lo_g, m), lo_g being the
-// smallest band+tail start of the group's heads.  Amend's band [m-r, m) is
-// cut off as its own segment, so Complete yields the rectification term
-// AS_{m-r+1:m} and the direct form of AS_{1:m-r} as by-products.  Chunks are
-// cut at multiples of C (a multiple of 16: page aligned).
+// smallest band+tail start of the group's heads.  In a MAC step Amend's band
+// [m-r, m) is cut off as its own segment, so Complete yields the
+// rectification term AS_{m-r+1:m} and the direct form of AS_{1:m-r} as
+// by-products: one work item per group, at the head of the list (item g is
+// group g's band).  The long segment [lo_g, m-r) (the whole span in a full
+// step) is cut into chunks at multiples of C (a multiple of 16: page
+// aligned); its items follow the bands, group after group.
 //
 // Balanced mode (Figure 3(b), "load-balanced planning"): every item costs at
 // most C tokens, so the step finishes when the longest item does; the plan
-// takes the smallest C for which the items fit one wave of the persistent
-// attention grid (or k waves when there are more segments than CTAs).
+// takes the smallest C for which the long items fit one wave of the
+// persistent attention grid (or k waves when there are more long segments
+// than CTAs).  The short band items either come on top -- a CTA that takes
+// one starts its long item that much later, which idle CTAs or the page
+// pools below absorb -- or are fitted into the wave, which lengthens every
+// long item by about nb / (P - nb); band_wave_fit picks the cheaper.
 // Longer spans thereby get proportionally more CTAs.  Equal mode gives every
 // group the same number of items whatever its span (unbalanced baseline).
 // ---------------------------------------------------------------------------
@@ -36,9 +43,22 @@ struct PlanShared {
     ChunkDiv cd;            // chunk_div(C) (balanced mode)
 };
 
+// End of the long segment [lo, sp); the band is [sp, hi) (empty in a full step).
 __device__ __forceinline__ int plan_split(const Layout &L, const StepArgs &a, int lo, int hi)
 {
-    return a.full_mode ? lo : max(lo, hi - L.band_r);
+    return a.full_mode ? hi : max(lo, hi - L.band_r);
+}
+
+// Band items at the head of the work list: one per group in a MAC step.
+__device__ __forceinline__ int plan_bands(const StepArgs &a, int nbg) { return a.full_mode ? 0 : nbg; }
+
+// Whether the nb band items share one wave of P CTAs with the long items
+// (TL long-segment tokens in all): fitting stretches a long item (about
+// TL / P tokens) by nb / (P - nb); on top, a CTA with two items runs about
+// band_r + 32 tokens longer (the band and an item's fixed cost).
+__device__ __forceinline__ bool band_wave_fit(int nb, long long TL, int P, int band_r)
+{
+    return nb > 0 && 2 * nb < P && (long long)nb * TL <= (long long)(band_r + 32) * P * (P - nb);
 }
 
 __device__ __forceinline__ int plan_chunk(const Layout &L, const StepArgs &a, const PlanShared &ps, int nbg, int lo,
@@ -62,13 +82,15 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
         lo = __ldcg(&L.grp_lo[lane]);
         sp = plan_split(L, a, lo, hi);
     }
-    long long T = lane < nbg ? hi - lo : 0, Tf = lane < nbg ? hi : 0;
-    int nseg = lane < nbg ? (sp > lo) + (hi > sp) : 0;
+    long long T = lane < nbg ? hi - lo : 0, Tf = lane < nbg ? hi : 0, TL = lane < nbg ? sp - lo : 0;
+    int nseg = lane < nbg ? (sp > lo) : 0;   // long segments
     for (int o = 16; o; o >>= 1) {
         T += __shfl_xor_sync(0xffffffffu, T, o);
         Tf += __shfl_xor_sync(0xffffffffu, Tf, o);
+        TL += __shfl_xor_sync(0xffffffffu, TL, o);
     }
     nseg = warp_sum_int(nseg);
+    const int nb = plan_bands(a, nbg);
     if (lane < nbg) {
         ps.lo[lane] = lo;
         ps.hi[lane] = hi;
@@ -79,11 +101,12 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
     if (a.plan_mode == 0) {
         const int P = a.grid_ctas;
         int Q = (4 * nseg <= P) ? P : P * (1 + (2 * nseg + P - 1) / P);
-        if (Q > L.item_cap) Q = L.item_cap;
+        if (Q == P && band_wave_fit(nb, TL, P, L.band_r)) Q = P - nb;
+        if (Q > L.item_cap - nb) Q = L.item_cap - nb;
         // The smallest fitting chunk is at least T / Q (count(C) >= T / C)
         // and at most T / (Q - 2 nseg) (count(C) < T / C + 2 nseg).  Float
         // quotients (relative error < 2^-22) widened by 2^-20 bracket both.
-        const float Tq = (float)T;
+        const float Tq = (float)TL;
         long long c_lo = (long long)(Tq / (float)Q * (1.f - 0x1p-20f)) / 16 * 16;
         long long c_hi = Q > 2 * nseg ? round_up16((long long)(Tq / (float)(Q - 2 * nseg) * (1.f + 0x1p-20f)) + 16)
                                       : (1ll << 30);
@@ -100,7 +123,7 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
 #pragma unroll 4
             for (int g = 0; g < nbg; g++) {
                 const int glo = ps.lo[g], ghi = ps.hi[g], gsp = plan_split(L, a, glo, ghi);
-                cnt += n_chunks_c(glo, gsp, R) + n_chunks_c(gsp, ghi, R);
+                cnt += n_chunks_c(glo, gsp, R);
             }
             const unsigned fit = __ballot_sync(0xffffffffu, cnt <= Q);
             const int k = fit ? __ffs(fit) - 1 : 31;
@@ -120,10 +143,9 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
     int cnt = 0;
     if (lane < nbg) {
         if (a.plan_mode == 0) {
-            cnt = n_chunks_c(lo, sp, RC) + n_chunks_c(sp, hi, RC);
+            cnt = n_chunks_c(lo, sp, RC);
         } else {
-            const int Cg = plan_chunk(L, a, ps, nbg, lo, hi);
-            cnt = n_chunks(lo, sp, Cg) + n_chunks(sp, hi, Cg);
+            cnt = n_chunks(lo, sp, plan_chunk(L, a, ps, nbg, lo, sp));
         }
     }
     int x = cnt;
@@ -132,8 +154,8 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
         const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    const int total = __shfl_sync(0xffffffffu, x, 31);
-    if (lane < nbg) ps.off[lane] = x - cnt;
+    const int total = nb + __shfl_sync(0xffffffffu, x, 31);
+    if (lane < nbg) ps.off[lane] = nb + x - cnt;
     if (lane == 0) {
         ps.off[nbg] = total;
         ps.total = total < L.item_cap ? total : L.item_cap;
@@ -159,18 +181,21 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
         ps.lo[bg] = __ldcg(&L.grp_lo[bg]);
     }
     __syncthreads();
+    const int nb = plan_bands(a, nbg);
     if (w == 0) {
-        long long T = 0, Tf = 0;
-        int nseg = 0;
+        long long T = 0, Tf = 0, TL = 0;
+        int nseg = 0;   // long segments
         for (int bg = lane; bg < nbg; bg += 32) {
             const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
             T += hi - lo;
             Tf += hi;
-            nseg += (sp > lo) + (hi > sp);
+            TL += sp - lo;
+            nseg += sp > lo;
         }
         for (int o = 16; o; o >>= 1) {
             T += __shfl_xor_sync(0xffffffffu, T, o);
             Tf += __shfl_xor_sync(0xffffffffu, Tf, o);
+            TL += __shfl_xor_sync(0xffffffffu, TL, o);
         }
         nseg = warp_sum_int(nseg);
         int C = kMinChunk;
@@ -180,16 +205,17 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
                 int c = 0;
                 for (int bg = lane; bg < nbg; bg += 32) {
                     const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
-                    c += n_chunks_c(lo, sp, R) + n_chunks_c(sp, hi, R);
+                    c += n_chunks_c(lo, sp, R);
                 }
                 return warp_sum_int(c);
             };
             const long long P = a.grid_ctas;
             long long Q = (4ll * nseg <= P) ? P : P * (1 + (2ll * nseg + P - 1) / P);
-            if (Q > L.item_cap) Q = L.item_cap;
-            // count(C) < T/C + 2 nseg, so C >= T / (Q - 2 nseg) always fits Q items
-            long long c_lo = round_up16((T + Q - 1) / Q);
-            long long c_hi = Q > 2ll * nseg ? round_up16((T + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg)) : (1ll << 30);
+            if (Q == P && band_wave_fit(nb, TL, (int)P, L.band_r)) Q = P - nb;
+            if (Q > L.item_cap - nb) Q = L.item_cap - nb;
+            // count(C) < TL/C + 2 nseg, so C >= TL / (Q - 2 nseg) always fits Q items
+            long long c_lo = round_up16((TL + Q - 1) / Q);
+            long long c_hi = Q > 2ll * nseg ? round_up16((TL + (Q - 2ll * nseg) - 1) / (Q - 2ll * nseg)) : (1ll << 30);
             if (c_lo < kMinChunk) c_lo = kMinChunk;
             if (c_hi < c_lo) c_hi = c_lo;
             // 32 candidates c_lo + 16 stride k (the last one c_hi, which fits):
@@ -237,28 +263,33 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
         if (bg < nbg) {
             const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
             if (a.plan_mode == 0) {
-                cnt = n_chunks_c(lo, sp, ps.cd) + n_chunks_c(sp, hi, ps.cd);
+                cnt = n_chunks_c(lo, sp, ps.cd);
             } else {
-                const int C = plan_chunk(L, a, ps, nbg, lo, hi);
-                cnt = n_chunks(lo, sp, C) + n_chunks(sp, hi, C);
+                cnt = n_chunks(lo, sp, plan_chunk(L, a, ps, nbg, lo, sp));
             }
         }
         int tot;
         const int off = base + block_exclusive_scan(cnt, &tot);
-        if (bg < nbg) ps.off[bg] = off;
+        if (bg < nbg) ps.off[bg] = nb + off;
         base += tot;
     }
     if (threadIdx.x == 0) {
-        ps.off[nbg] = base;
-        ps.total = base < L.item_cap ? base : L.item_cap;
+        ps.off[nbg] = nb + base;
+        ps.total = nb + base < L.item_cap ? nb + base : L.item_cap;
     }
     __syncthreads();
 }
 
-// Work item `it` of the plan: {group, lo, hi, segment}.
+// Work item `it` of the plan: {group, lo, hi, segment}.  Items 0 .. nb - 1
+// are the groups' bands (segment 1), then come the long segments' chunks
+// (segment 0) group after group.
 __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &ps, int nbg, int it)
 {
-    int g0 = 0, g1 = nbg - 1;   // the last group whose first item is <= it
+    if (it < plan_bands(a, nbg)) {
+        const int lo = ps.lo[it], hi = ps.hi[it];
+        return make_int4(it, plan_split(L, a, lo, hi), hi, 1);
+    }
+    int g0 = 0, g1 = nbg - 1;   // the last group whose first long item is <= it
     while (g0 < g1) {
         const int mid = (g0 + g1 + 1) >> 1;
         if (ps.off[mid] <= it) g0 = mid;
@@ -266,15 +297,10 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
     }
     const int bg = g0, k = it - ps.off[bg];
     const int lo = ps.lo[bg], hi = ps.hi[bg], sp = plan_split(L, a, lo, hi);
-    const int C = plan_chunk(L, a, ps, nbg, lo, hi);
+    const int C = plan_chunk(L, a, ps, nbg, lo, sp);
     const ChunkDiv R = a.plan_mode == 0 ? ps.cd : chunk_div(C);
-    const int nA = n_chunks_c(lo, sp, R);
-    if (k < nA) {
-        const int c = div_c(lo, R) + k;
-        return make_int4(bg, max(lo, c * C), min(sp, (c + 1) * C), 0);
-    }
-    const int c = div_c(sp, R) + (k - nA);
-    return make_int4(bg, max(sp, c * C), min(hi, (c + 1) * C), 1);
+    const int c = div_c(lo, R) + k;
+    return make_int4(bg, max(lo, c * C), min(sp, (c + 1) * C), 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -473,14 +499,14 @@ __global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : 
         const int npg = pg1 - pg0 + 1;
 
         // Pages.  Every long item of the segment keeps its last ~8 % of pages
-        // back in a pool shared by the segment's CTAs (not for 32-head
-        // groups, whose CTAs hold a single page lane): a CTA streams its own
+        // back in a pool shared by the segment's CTAs (not with four 8-head
+        // tiles, whose CTAs hold a single page lane): a CTA streams its own
         // other pages (this lane: pg0 + pl + k NP), then claims pool pages one
         // at a time, so the CTAs of a segment finish together whatever
         // bandwidth each one gets.  Items of the segment are the C-aligned
         // chunks c_first, c_first + 1, ... of [slo, shi).
         constexpr int KDF = NH <= 2 ? kDynFrac : 0;
-        const int Cg = plan_chunk(L, a, ps, nbg, glo, ghi);
+        const int Cg = plan_chunk(L, a, ps, nbg, glo, gsp);
         const ChunkDiv Rg = a.plan_mode == 0 ? ps.cd : chunk_div(Cg);
         const int c_first = div_c(slo, Rg), n_seg = div_c(shi - 1, Rg) - c_first + 1;
         auto chunk_pages = [&](int j, int &p0, int &p1) {
@@ -488,7 +514,10 @@ __global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : 
             p0 = max(slo, c * Cg) >> 4;
             p1 = (min(shi, (c + 1) * Cg) - 1) >> 4;
         };
-        auto kept_back = [&](int n) { return (KDF > 0 && n >= kDynMinPages) ? max(2, n * KDF / 128) : 0; };
+        // (a band item is a segment of its own: nothing is kept back)
+        auto kept_back = [&](int n) {
+            return (KDF > 0 && item.w == 0 && n >= kDynMinPages) ? max(2, n * KDF / 128) : 0;
+        };
         int fp0, fp1, lp0 = 0, lp1 = -1;
         chunk_pages(0, fp0, fp1);
         if (n_seg > 1) chunk_pages(n_seg - 1, lp0, lp1);

@@ -386,8 +386,13 @@ __global__ void __launch_bounds__(NW * 32) combine_kernel(Layout L, StepArgs a)
 
     float m_ring = NEG;
     float4 o_ring = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 ml_band = make_float2(NEG, 0.f);
+    float4 o_band = make_float4(0.f, 0.f, 0.f, 0.f);
     int m = 0, slot = 0;
     if (!a.full_mode && w == 0) {
+        // the group's band item (item bg of a MAC step's plan) seeds the band sums
+        ml_band = L.part_ml[(size_t)bg * L.G + hh];
+        o_band = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)bg * L.G + hh) * kD + 4 * lane);
         m = L.m_cur[b];   // for the epilogue, loaded alongside the rest
         slot = L.slot_cur[b];
         const int eff = L.dec_slot[gw];
@@ -402,9 +407,10 @@ __global__ void __launch_bounds__(NW * 32) combine_kernel(Layout L, StepArgs a)
         }
     }
     const int off0 = L.grp_item_off[bg], off1 = L.grp_item_off[bg + 1];
-    // One pass: each warp merges items w, w + NW, ... (segment 0
-    // and segment 1 separately) online, rescaling its sums when a batch
-    // raises a maximum; a shared-memory step then merges the warps.
+    // One pass: each warp merges the group's long-segment items w, w + NW, ...
+    // online, rescaling its sums when a batch raises a maximum; a
+    // shared-memory step then merges the warps.  The band (segment 1) is
+    // the single item bg, which seeds warp 0's band sums.
     float mp = NEG, mb = NEG, lp = 0.f, lb = 0.f;
     float4 op = make_float4(0.f, 0.f, 0.f, 0.f), ob = op;
     if (w == 0 && m_ring != NEG) {   // the reused AS_{1:p-r}: weight 1 at its own maximum
@@ -412,49 +418,37 @@ __global__ void __launch_bounds__(NW * 32) combine_kernel(Layout L, StepArgs a)
         lp = 1.f;
         op = o_ring;
     }
+    if (w == 0 && ml_band.x != NEG) {
+        mb = ml_band.x;
+        lb = ml_band.y;
+        ob = o_band;
+    }
     constexpr int kBatch = KB;
     for (int i0 = off0 + w; i0 < off1; i0 += kBatch * NW) {
         float2 ml[kBatch];
-        int sg[kBatch];
         float4 ov[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; k++) {
             const int i = min(i0 + k * NW, off1 - 1);
             ml[k] = L.part_ml[(size_t)i * L.G + hh];
-            sg[k] = L.items[i].w;
             ov[k] = *reinterpret_cast<const float4 *>(L.part_o + ((size_t)i * L.G + hh) * kD + 4 * lane);
             if (i0 + k * NW >= off1) ml[k].x = NEG;   // padding slot
         }
-        float np = mp, nb = mb;
+        float np = mp;
 #pragma unroll
-        for (int k = 0; k < kBatch; k++) {
-            if (sg[k]) nb = fmaxf(nb, ml[k].x);
-            else np = fmaxf(np, ml[k].x);
-        }
+        for (int k = 0; k < kBatch; k++) np = fmaxf(np, ml[k].x);
         if (np != mp) {
             const float r = mp == NEG ? 0.f : exp2f(mp - np);
             lp *= r;
             op = scale4(op, r);
             mp = np;
         }
-        if (nb != mb) {
-            const float r = mb == NEG ? 0.f : exp2f(mb - nb);
-            lb *= r;
-            ob = scale4(ob, r);
-            mb = nb;
-        }
 #pragma unroll
         for (int k = 0; k < kBatch; k++) {
             if (ml[k].x == NEG) continue;
-            if (sg[k]) {
-                const float wi = exp2f(ml[k].x - mb);
-                lb = fmaf(ml[k].y, wi, lb);
-                fma4(ob, wi, ov[k]);
-            } else {
-                const float wi = exp2f(ml[k].x - mp);
-                lp = fmaf(ml[k].y, wi, lp);
-                fma4(op, wi, ov[k]);
-            }
+            const float wi = exp2f(ml[k].x - mp);
+            lp = fmaf(ml[k].y, wi, lp);
+            fma4(op, wi, ov[k]);
         }
     }
     if (lane == 0) {

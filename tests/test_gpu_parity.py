@@ -168,15 +168,16 @@ def test_reset_request_restarts_cleanly():
 
 
 def test_plan_fits_one_wave_of_the_grid():
-    """Balanced planning keeps the work list within the persistent grid when
-    there are few segments, so no CTA runs a second item."""
+    """Balanced planning keeps the long-segment items within one wave of the
+    persistent grid when there are few groups; each group's band is one more
+    item on top (a CTA that takes one starts its long item a band later)."""
     c = cfg(batch=1, context=20000, steps=3, rho=0.5)
     p = _pair(c)
     for t in range(3):
         p.mac_step(t, force=True, check_ring=False)
     st = p.mac.stats()
     grid = torch.cuda.get_device_properties(0).multi_processor_count * 2
-    assert st["work_items"] / st["steps"] <= grid
+    assert st["work_items"] / st["steps"] <= grid + c.batch * c.kv_heads
 
 
 @pytest.mark.parametrize("amend_band", [0, 1])
