@@ -859,8 +859,8 @@ def bench_match_windows(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ctx, steps, warm = 32768, args.steps, args.warmup
-    for kv in (1, 8):
-        for L in (16, 64, 256, 512, 1024, 2048):
+    for kv in [int(x) for x in args.match_kv_heads.split(",")]:
+        for L in [int(x) for x in args.match_windows.split(",")]:
             cfg = W.DecodeConfig(f"match_window_gqa32x{kv}_ctx{ctx}_L{L}", 1, 32, kv, 128, ctx, warm + steps + 1, L, 64,
                                  0.3, rho=0.95, paged=True, seed=20260331 + 6)
             mac = MacAttention(32, kv, 128, L, 64, 0.3, max_batch=1, max_ctx=ctx + warm + steps + 8, page_size=16)
@@ -995,6 +995,8 @@ def main():
     ap.add_argument("--sweep-batches", default="1,8,32")
     ap.add_argument("--sweep-rates", default="0,0.5,0.9,1.0")
     ap.add_argument("--sweep-kv-heads", default="1,8")
+    ap.add_argument("--match-windows", default="16,64,256,512,1024,2048", help="ring lengths of match_windows")
+    ap.add_argument("--match-kv-heads", default="1,8", help="KV heads (32 q heads) of match_windows")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

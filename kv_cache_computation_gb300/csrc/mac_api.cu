@@ -11,6 +11,7 @@
 #include "../../include/mac.h"
 #include "mac_internal.cuh"
 
+#include <algorithm>
 #include <chrono>
 #include <cmath>
 #include <cstdio>
@@ -136,6 +137,7 @@ struct mac_ctx {
     Layout lay;
     int device = 0;
     int grid_ctas = 0;
+    int grid_ctas_wide = 0;   // grid of the attention variant for steps of many groups (0: none)
     size_t attn_smem = 0;
     cudaStream_t side = nullptr;
     cudaEvent_t ev_complete = nullptr, ev_amend = nullptr;
@@ -292,7 +294,8 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
     a.lse_out = lse_out;
     a.force = (!full && h->force_next) ? 1 : 0;
     a.full_mode = full ? 1 : 0;
-    a.grid_ctas = h->grid_ctas;
+    a.wide = (h->grid_ctas_wide > 0 && attention_wide(h->lay.G, batch * h->lay.Hkv)) ? 1 : 0;
+    a.grid_ctas = a.wide ? h->grid_ctas_wide : h->grid_ctas;
     a.plan_mode = h->cfg.plan_mode;
     h->force_next = false;
 
@@ -415,13 +418,19 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     if (e != cudaSuccess) return fail(e, "cudaGetDeviceProperties");
     if (prop.major * 10 + prop.minor != 103) return fail(cudaErrorNoKernelImageForDevice, "device check (sm_103a required)");
     int per_sm = 0;
-    e = attention_kernel_config(z.G, &h->attn_smem, &per_sm);
+    e = attention_kernel_config(z.G, false, &h->attn_smem, &per_sm);
     if (e != cudaSuccess) return fail(e, "attention kernel configuration");
     if (per_sm < 1) return fail(cudaErrorInvalidConfiguration, "attention kernel occupancy");
+    h->grid_ctas = std::min(prop.multiProcessorCount * per_sm, kMaxCtas);
+    if (attention_wide(z.G, kMaxGroupsPerStep)) {
+        size_t smem_w = 0;
+        e = attention_kernel_config(z.G, true, &smem_w, &per_sm);
+        if (e != cudaSuccess) return fail(e, "attention kernel configuration");
+        if (per_sm < 1 || smem_w != h->attn_smem) return fail(cudaErrorInvalidConfiguration, "attention kernel occupancy");
+        h->grid_ctas_wide = std::min(prop.multiProcessorCount * per_sm, kMaxCtas);
+    }
     e = amend_kernel_config();
     if (e != cudaSuccess) return fail(e, "amend kernel configuration");
-    h->grid_ctas = prop.multiProcessorCount * per_sm;
-    if (h->grid_ctas > kMaxCtas) h->grid_ctas = kMaxCtas;
 
     char *kv = (char *)dev_kv, *rg = (char *)dev_ring, *sc = (char *)dev_scratch;
     Layout &L = h->lay;

@@ -328,8 +328,8 @@ __device__ int4 plan_item(const Layout &L, const StepArgs &a, const PlanShared &
 //   O[16 heads x 128]   += P[16 x 16] V[16 x 128]        16 x 2 mma (hi + lo)
 // with Q in registers as A fragments and K, V read by ldmatrix as B.
 // ---------------------------------------------------------------------------
-template <int NW, int S, int NH, bool HM>
-__global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : MAC_HM_MIN_CTAS_32) : 1) attention_kernel(Layout L, StepArgs a)
+template <int NW, int S, int NH, bool HM, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB) attention_kernel(Layout L, StepArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int NP = NW / NH;
@@ -640,7 +640,9 @@ __global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : 
                 // S = Q K^T: n-tile j holds tokens 8 j .. 8 j + 7; this thread
                 // has head rows r4 (sc[j][0..1]) and r4 + 8 (sc[j][2..3]) at
                 // tokens 8 j + 2 c4, + 1
-                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // (even and odd k-steps accumulate apart: four independent
+                // mma chains instead of two)
+                float sc[2][2][4] = {};
                 {
                     const uint32_t kbase = Ks + vtok * 256;
 #pragma unroll
@@ -648,15 +650,15 @@ __global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : 
                         const int ch = 2 * kk + ((lane >> 3) & 1);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4(b0, b1, b2, b3, kbase + ((ch ^ (vtok & 7)) << 4));
-                        mma_bf16(sc[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-                        mma_bf16(sc[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+                        mma_bf16(sc[0][kk & 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+                        mma_bf16(sc[1][kk & 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
                     }
                 }
                 float z[2][4];
 #pragma unroll
                 for (int j = 0; j < 2; j++)
 #pragma unroll
-                    for (int e = 0; e < 4; e++) z[j][e] = sc[j][e] * sl2;
+                    for (int e = 0; e < 4; e++) z[j][e] = (sc[j][0][e] + sc[j][1][e]) * sl2;
                 if (pg * 16 < lo_max || pg * 16 + 16 > shi) {
 #pragma unroll
                     for (int j = 0; j < 2; j++)
@@ -716,17 +718,25 @@ __global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : 
                         plo[2 * j + rr] = bf16x2_bits(lv);
                     }
                 // O += P V: ldmatrix.trans gives the B fragments of dim
-                // n-tiles 2 np and 2 np + 1
+                // n-tiles 2 np and 2 np + 1; four n-tiles per round, hi parts
+                // then lo parts, so no mma waits on the one before it
                 const uint32_t vbase = Vs + krow * 256;
 #pragma unroll
-                for (int np = 0; np < 8; np++) {
-                    const int ch = 2 * np + (lane >> 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(b0, b1, b2, b3, vbase + ((ch ^ (krow & 7)) << 4));
-                    mma_bf16(acc[2 * np], ph[0], ph[1], ph[2], ph[3], b0, b1);
-                    mma_bf16(acc[2 * np], plo[0], plo[1], plo[2], plo[3], b0, b1);
-                    mma_bf16(acc[2 * np + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-                    mma_bf16(acc[2 * np + 1], plo[0], plo[1], plo[2], plo[3], b2, b3);
+                for (int np = 0; np < 8; np += 2) {
+                    uint32_t b[2][4];
+#pragma unroll
+                    for (int u = 0; u < 2; u++) {
+                        const int ch = 2 * (np + u) + (lane >> 4);
+                        ldsm_x4_t(b[u][0], b[u][1], b[u][2], b[u][3], vbase + ((ch ^ (krow & 7)) << 4));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; u++)
+                        mma_bf16(acc[2 * np + u], ph[0], ph[1], ph[2], ph[3], b[u >> 1][2 * (u & 1)],
+                                 b[u >> 1][2 * (u & 1) + 1]);
+#pragma unroll
+                    for (int u = 0; u < 4; u++)
+                        mma_bf16(acc[2 * np + u], plo[0], plo[1], plo[2], plo[3], b[u >> 1][2 * (u & 1)],
+                                 b[u >> 1][2 * (u & 1) + 1]);
                 }
                 continue;
             }
@@ -947,33 +957,42 @@ __global__ void __launch_bounds__(NW * 32, HM ? (NH == 1 ? MAC_HM_MIN_CTAS_16 : 
 static bool heads_on_m(int G) { return kHeadsOnM && !kAttnCudaCore && G % 16 == 0; }
 static int head_tiles(int G) { return heads_on_m(G) ? G / 16 : (G + 7) / 8; }
 
+// Pipeline stages per page lane: 32-head groups (two page lanes per CTA)
+// take their own depth.
+static int attention_stages(int G) { return heads_on_m(G) && G == 32 ? kHmStages32 : kAttnStages; }
+
 static size_t attention_smem(int G)
 {
     const int NH = head_tiles(G), NP = kAttnWarps / NH;
-    const size_t pipe = (size_t)NP * kAttnStages * kStageBytes;
+    const size_t pipe = (size_t)NP * attention_stages(G) * kStageBytes;
     const size_t red = (size_t)NP * G * kD * 4 + (size_t)NP * G * 8;
     const size_t q_tiles = kAttnCudaCore ? (size_t)NH * 8 * kD * 2 : 0;   // after the stages
     return (pipe > red ? pipe : red) + q_tiles;
 }
 
-template <int NH, bool HM>
+template <int NH, bool HM, int S, int MINB>
 static cudaError_t attention_config_nh(size_t smem, int *ctas_per_sm)
 {
-    auto k = attention_kernel<kAttnWarps, kAttnStages, NH, HM>;
+    auto k = attention_kernel<kAttnWarps, S, NH, HM, MINB>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, k, kAttnWarps * 32, smem);
 }
 
-cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm)
+bool attention_wide(int G, int groups) { return heads_on_m(G) && G == 32 && groups >= kHmWideGroups; }
+
+cudaError_t attention_kernel_config(int G, bool wide, size_t *smem, int *ctas_per_sm)
 {
     *smem = attention_smem(G);
-    if (heads_on_m(G)) return G == 16 ? attention_config_nh<1, true>(*smem, ctas_per_sm)
-                                      : attention_config_nh<2, true>(*smem, ctas_per_sm);
+    if (heads_on_m(G)) {
+        if (G == 16) return attention_config_nh<1, true, kAttnStages, kHmMinCtas16>(*smem, ctas_per_sm);
+        if (wide) return attention_config_nh<2, true, kHmStages32, kHmMinCtas32Wide>(*smem, ctas_per_sm);
+        return attention_config_nh<2, true, kHmStages32, kHmMinCtas32>(*smem, ctas_per_sm);
+    }
     switch (head_tiles(G)) {
-    case 1: return attention_config_nh<1, false>(*smem, ctas_per_sm);
-    case 2: return attention_config_nh<2, false>(*smem, ctas_per_sm);
-    default: return attention_config_nh<4, false>(*smem, ctas_per_sm);
+    case 1: return attention_config_nh<1, false, kAttnStages, 1>(*smem, ctas_per_sm);
+    case 2: return attention_config_nh<2, false, kAttnStages, 1>(*smem, ctas_per_sm);
+    default: return attention_config_nh<4, false, kAttnStages, 1>(*smem, ctas_per_sm);
     }
 }
 
@@ -982,13 +1001,18 @@ cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cu
     const dim3 grid(a.grid_ctas), block(kAttnWarps * 32);
     if (heads_on_m(L.G)) {
         if (L.G == 16)
-            return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1, true>, grid, block, smem, s, a.pdl, L, a);
-        return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2, true>, grid, block, smem, s, a.pdl, L, a);
+            return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1, true, kHmMinCtas16>, grid, block, smem, s,
+                                    a.pdl, L, a);
+        if (a.wide)
+            return launch_maybe_pdl(attention_kernel<kAttnWarps, kHmStages32, 2, true, kHmMinCtas32Wide>, grid, block, smem,
+                                    s, a.pdl, L, a);
+        return launch_maybe_pdl(attention_kernel<kAttnWarps, kHmStages32, 2, true, kHmMinCtas32>, grid, block, smem, s,
+                                a.pdl, L, a);
     }
     switch (head_tiles(L.G)) {
-    case 1: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1, false>, grid, block, smem, s, a.pdl, L, a);
-    case 2: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2, false>, grid, block, smem, s, a.pdl, L, a);
-    default: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 4, false>, grid, block, smem, s, a.pdl, L, a);
+    case 1: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 1, false, 1>, grid, block, smem, s, a.pdl, L, a);
+    case 2: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 2, false, 1>, grid, block, smem, s, a.pdl, L, a);
+    default: return launch_maybe_pdl(attention_kernel<kAttnWarps, kAttnStages, 4, false, 1>, grid, block, smem, s, a.pdl, L, a);
     }
 }
 

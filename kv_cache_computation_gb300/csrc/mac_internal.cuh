@@ -61,15 +61,31 @@ constexpr bool kAttnCudaCore = MAC_ATTN_CUDA_CORE != 0;
 // Groups of 16 and 32 heads take the heads-on-M attention tiles (0: the
 // 8-head N tiles of smaller groups for every group size; comparison build).
 constexpr bool kHeadsOnM = MAC_ATTN_HEADS_ON_M != 0;
-// Resident CTAs per SM the heads-on-M kernel is register-budgeted for: 2 for
-// 16-head groups (one 16-head tile per warp, 4 page lanes), 3 for 32-head
-// groups (2 tiles, 2 page lanes; ~170 registers, a few bytes spilled).
+// Resident CTAs per SM the heads-on-M kernel is register-budgeted for: 2
+// (no spills) for 16-head groups and, with fewer than kHmWideGroups groups
+// in the step, for 32-head groups; 3 (about 170 registers, a few bytes
+// spilled; more warps to hide latency) for 32-head groups in steps of many
+// groups, which stream the most pages per CTA.
 #ifndef MAC_HM_MIN_CTAS_16
 #define MAC_HM_MIN_CTAS_16 2
 #endif
 #ifndef MAC_HM_MIN_CTAS_32
-#define MAC_HM_MIN_CTAS_32 3
+#define MAC_HM_MIN_CTAS_32 2
 #endif
+#ifndef MAC_HM_MIN_CTAS_32_WIDE
+#define MAC_HM_MIN_CTAS_32_WIDE 3
+#endif
+#ifndef MAC_HM_WIDE_GROUPS
+#define MAC_HM_WIDE_GROUPS 32
+#endif
+constexpr int kHmMinCtas16 = MAC_HM_MIN_CTAS_16;
+constexpr int kHmMinCtas32 = MAC_HM_MIN_CTAS_32;
+constexpr int kHmMinCtas32Wide = MAC_HM_MIN_CTAS_32_WIDE;
+constexpr int kHmWideGroups = MAC_HM_WIDE_GROUPS;
+#ifndef MAC_HM_STAGES_32
+#define MAC_HM_STAGES_32 3
+#endif
+constexpr int kHmStages32 = MAC_HM_STAGES_32;   // pipeline stages per page lane, 32-head groups
 constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
 constexpr int kMinChunk = 64;           // smallest work-item span in tokens
 constexpr int kPlanCache = 1024;        // groups the planner caches in shared memory
@@ -150,6 +166,7 @@ struct StepArgs {
     int grid_ctas;    // attention CTAs
     int plan_mode;    // 0 balanced, 1 equal split per group
     int pdl;          // launch attention / combine as programmatic dependents
+    int wide;         // attention: the variant for many groups (grid_ctas is its grid)
 };
 
 // launchers (mac_kernels.cu)
@@ -161,7 +178,8 @@ cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_append(const Layout &L, int req, int start, int n, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, cudaStream_t s);
-cudaError_t attention_kernel_config(int G, size_t *smem, int *ctas_per_sm);
+cudaError_t attention_kernel_config(int G, bool wide, size_t *smem, int *ctas_per_sm);
+bool attention_wide(int G, int groups);   // whether a step of `groups` groups takes the wide variant
 cudaError_t amend_kernel_config();
 
 }  // namespace macgpu

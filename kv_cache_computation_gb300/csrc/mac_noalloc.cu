@@ -128,7 +128,7 @@ mac_status setup_device(int dev, DeviceSetup **out)
         const int groups[6] = {1, 2, 4, 8, 16, 32};
         for (int i = 0; i < 6; i++) {
             int per_sm = 0;
-            if (attention_kernel_config(groups[i], &s.smem[i], &per_sm) != cudaSuccess || per_sm < 1)
+            if (attention_kernel_config(groups[i], false, &s.smem[i], &per_sm) != cudaSuccess || per_sm < 1)
                 return MAC_ERR_CUDA;
             s.ctas[i] = s.sm_count * per_sm < kMaxCtas ? s.sm_count * per_sm : kMaxCtas;
         }
