@@ -896,56 +896,110 @@ def bench_match_windows(args, ws, rank, local):
     return None
 
 
+def _prefix_summaries(Kp, Vp, q_post, pos, band_r, G, scale):
+    """AS_{1:pos-r} of prefill queries (what the caller's prefill attention
+    yields for the ring entries it seeds), in fp64 on the GPU: Kp, Vp bf16
+    [T, Hkv, d] of one request; q_post bf16 [n, H, d]; pos 1-based [n].
+    Returns o fp32 [n, H, d], lse fp32 [n, H] (AS_empty = (0, -inf))."""
+    n, H, d = q_post.shape
+    K = Kp.double().repeat_interleave(G, dim=1).transpose(0, 1)          # [H, T, d]
+    V = Vp.double().repeat_interleave(G, dim=1).transpose(0, 1)
+    q = q_post.double().transpose(0, 1)                                  # [H, n, d]
+    z = torch.matmul(q, K.transpose(1, 2)) * scale                      # [H, n, T]
+    T = K.shape[1]
+    lim = torch.as_tensor(pos, device=z.device) - band_r                # tokens [0, pos - r)
+    mask = torch.arange(T, device=z.device)[None, :] < lim[:, None]
+    z = torch.where(mask[None], z, torch.full_like(z, -math.inf))
+    lse = torch.logsumexp(z, dim=-1)                                     # [H, n]
+    w = torch.exp(z - torch.where(torch.isfinite(lse), lse, torch.zeros_like(lse))[..., None])
+    o = torch.matmul(w, V)                                               # [H, n, d]
+    return o.transpose(0, 1).float().contiguous(), lse.transpose(0, 1).float().contiguous()
+
+
 def bench_rectification(args, ws, rank, local):
-    """Synthetic analogue of the paper's Figures 4 and 5: on AR(1) query
-    streams, the MAC output against full attention (both on this GPU, same
-    inputs) by reuse gap and band width, and hit rate / skipped-prefix
-    fraction against the threshold and the window.  One JSON line per point."""
+    """Synthetic analogue of the paper's Figures 4 and 5: the MAC output
+    against full attention (both on this GPU, same inputs).  Three studies,
+    one JSON line per point:
+      tau_band -- AR(1) streams: hit rate, skipped prefix and error by reuse
+                  gap over threshold x window x band;
+      gap      -- streams that recur at a chosen gap (q~_t = q~_{t-gap} +
+                  0.1 eps): error by reuse gap x band (Figure 4);
+      window   -- topic-revisiting streams with the ring seeded from prefill
+                  queries: acceptance, skipped prefix and KV read vs window
+                  at a fixed threshold (Figure 5, bottom row)."""
     from kv_cache_computation_gb300 import MacAttention
     from kv_cache_computation_gb300 import workloads as W
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ctx, steps = 8192, args.steps
-    for rho in (0.95, 0.99):
-        for tau in (0.2, 0.3, 0.4, 0.5):
-            for L in (4, 16, 64):
-                for r in (16, 64, 256):
-                    cfg = W.DecodeConfig(f"rect_rho{rho}_tau{tau}_L{L}_r{r}", 1, 32, 8, 128, ctx, steps, L, r, tau,
-                                         rho=rho, paged=False, seed=20260331 + 7)
-                    mk = lambda: MacAttention(32, 8, 128, L, r, tau, max_batch=1, max_ctx=ctx + steps + 1, page_size=0)
-                    mac, full = mk(), mk()
-                    Kp, Vp = W.prefill_kv(cfg, device=dev)
-                    mac.append_kv(0, Kp[0], Vp[0])
-                    full.append_kv(0, Kp[0], Vp[0])
-                    inp = W.decode_inputs(cfg, device=dev)
-                    errs = {}
-                    hits = skipped = total = 0
-                    for t in range(steps):
-                        a = [inp[k][t] for k in ("q_pre", "q_post", "k_new", "v_new")]
-                        o_mac, _ = mac.decode_step(*a)
-                        o_full, _ = full.full_step(*a[1:])
-                        dec = mac.decisions(1)
-                        pos = mac.read_ring(0)["pos"] if dec["hit"].any() else None
-                        e = ((o_mac.float() - o_full.float()).abs().amax(-1) /
-                             o_full.float().abs().amax(-1)).cpu().numpy()[0]
-                        m = ctx + t + 1
-                        for h in range(32):
-                            total += 1
-                            if dec["hit"][0, h]:
-                                hits += 1
-                                p = int(pos[dec["slot"][0, h]]) if pos is not None else m
-                                gap = m - p
-                                skipped += max(0, p - r)
-                                errs.setdefault(gap, []).append(float(e[h]))
-                    mac.close()
-                    full.close()
-                    if rank == 0:
-                        print(json.dumps({"workload": "rectification_study", "rho": rho, "tau": tau, "window": L,
-                                          "band_r": r, "context": ctx, "steps": steps,
-                                          "hit_rate": round(hits / total, 4),
-                                          "skipped_prefix_fraction": round(skipped / (total * (ctx + steps / 2)), 4),
-                                          "error_by_gap": {str(k): [round(float(np.mean(v)), 6), len(v)]
-                                                           for k, v in sorted(errs.items())}}), flush=True)
+    studies = args.rect_studies.split(",")
+
+    def run(cfg, seed_n=0):
+        L, r, tau = cfg.ring_len, cfg.band_r, cfg.tau
+        mk = lambda: MacAttention(cfg.heads, cfg.kv_heads, 128, L, r, tau, max_batch=1,
+                                  max_ctx=ctx + cfg.steps + 1, page_size=0)
+        mac, full = mk(), mk()
+        Kp, Vp = W.prefill_kv(cfg, device=dev)
+        mac.append_kv(0, Kp[0], Vp[0])
+        full.append_kv(0, Kp[0], Vp[0])
+        if seed_n:
+            q_pre, q_post = W.prefill_queries(cfg, device=dev)
+            pos = list(range(ctx - seed_n + 1, ctx + 1))
+            o, lse = _prefix_summaries(Kp[0], Vp[0], q_post[:, 0], pos, r, cfg.group, 1 / math.sqrt(128))
+            mac.seed_ring(0, q_pre[:, 0].contiguous(), o, lse, pos)
+        inp = W.decode_inputs(cfg, device=dev)
+        errs, hits, skipped, total = {}, 0, 0.0, 0
+        mac.reset_stats()
+        for t in range(cfg.steps):
+            a = [inp[k][t] for k in ("q_pre", "q_post", "k_new", "v_new")]
+            pos = mac.read_ring(0)["pos"]      # before the step: its insert may overwrite the matched entry
+            o_mac, _ = mac.decode_step(*a)
+            o_full, _ = full.full_step(*a[1:])
+            dec = mac.decisions(1)
+            e = ((o_mac.float() - o_full.float()).abs().amax(-1) / o_full.float().abs().amax(-1)).cpu().numpy()[0]
+            m = ctx + t + 1
+            for h in range(cfg.heads):
+                total += 1
+                if dec["hit"][0, h]:
+                    hits += 1
+                    p = int(pos[dec["slot"][0, h]])
+                    skipped += max(0, p - r) / m
+                    errs.setdefault(m - p, []).append(float(e[h]))
+        st = mac.stats()
+        mac.close()
+        full.close()
+        return {"hit_rate": round(hits / total, 4), "skipped_prefix_fraction": round(skipped / total, 4),
+                "kv_bytes_read_vs_full": round(st["kv_tokens_read"] / max(1, st["kv_tokens_full"]), 4),
+                "mean_error_on_hits": round(float(np.mean([x for v in errs.values() for x in v])), 6) if hits else None,
+                "error_by_gap": {str(k): [round(float(np.mean(v)), 6), len(v)] for k, v in sorted(errs.items())}}
+
+    def emit(line):
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+
+    if "tau_band" in studies:
+        for rho in (0.95, 0.99):
+            for tau in (0.2, 0.3, 0.4, 0.5):
+                for L in (4, 16, 64):
+                    for r in (16, 64, 256):
+                        cfg = W.DecodeConfig(f"rect_rho{rho}_tau{tau}_L{L}_r{r}", 1, 32, 8, 128, ctx, steps, L, r, tau,
+                                             rho=rho, paged=False, seed=20260331 + 7)
+                        emit({"workload": "rectification_study", "study": "tau_band", "rho": rho, "tau": tau,
+                              "window": L, "band_r": r, "context": ctx, "steps": steps, **run(cfg)})
+    if "gap" in studies:
+        for gap in (1, 2, 4, 8, 16, 32):
+            for r in (16, 64, 256):
+                cfg = W.DecodeConfig(f"rect_gap{gap}_r{r}", 1, 32, 8, 128, ctx, steps, 32, r, 0.3, gap=gap,
+                                     gap_noise=0.1, paged=False, seed=20260331 + 8)
+                emit({"workload": "rectification_study", "study": "gap", "gap": gap, "gap_noise": 0.1, "tau": 0.3,
+                      "window": 32, "band_r": r, "context": ctx, "steps": steps, **run(cfg)})
+    if "window" in studies:
+        for L in (16, 64, 256, 1024):
+            cfg = W.DecodeConfig(f"rect_topics_L{L}", 1, 32, 8, 128, ctx, steps, L, 64, 0.3, topics=32,
+                                 topic_stay=0.9, topic_noise=0.1, lead=L, paged=False, seed=20260331 + 9)
+            emit({"workload": "rectification_study", "study": "window", "window": L, "tau": 0.3, "band_r": 64,
+                  "topics": 32, "topic_stay": 0.9, "seeded_entries": L, "context": ctx, "steps": steps,
+                  **run(cfg, seed_n=L)})
     return None
 
 
@@ -996,6 +1050,7 @@ def main():
     ap.add_argument("--sweep-rates", default="0,0.5,0.9,1.0")
     ap.add_argument("--sweep-kv-heads", default="1,8")
     ap.add_argument("--match-windows", default="16,64,256,512,1024,2048", help="ring lengths of match_windows")
+    ap.add_argument("--rect-studies", default="tau_band,gap,window", help="studies of the rectification workload")
     ap.add_argument("--match-kv-heads", default="1,8", help="KV heads (32 q heads) of match_windows")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -559,20 +559,43 @@ __global__ void __launch_bounds__(1024) amend_kernel(Layout L, StepArgs a)
         bool ok = true;
         float M = NEG, Ls = 0.f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        __shared__ long long s_page[kBandTile / kPage + 1];   // element offset of each page of a tile (-1: refused)
         for (int t0 = m - r; t0 < m; t0 += kBandTile) {
             const int n = min(kBandTile, m - t0);
+            const int p_first = t0 >> 4, npages = ((t0 + n - 1) >> 4) - p_first + 1;
             __syncthreads();   // previous tile consumed
-            for (int c = threadIdx.x; c < n * 32; c += blockDim.x) {
-                const int tok = c >> 5, part = c & 31, isv = part >> 4, ch = part & 15;
-                bool okc = true;
-                const int j = t0 + tok;
-                const size_t off = kv_block(L, b, g, j >> 4, okc) + (size_t)(j & 15) * kD;
-                if (!okc) {
-                    ok = false;
-                    continue;
+            if ((int)threadIdx.x < npages) {   // one page-table lookup per page of the tile
+                bool okp = true;
+                const size_t o = kv_block(L, b, g, p_first + threadIdx.x, okp);
+                s_page[threadIdx.x] = okp ? (long long)o : -1ll;
+            }
+            __syncthreads();
+            // 16-byte chunks c = token * 32 + part (parts 0-15 K, 16-31 V): each
+            // thread issues eight loads before it stores any of them
+            const int total = n * 32;
+            for (int c0 = threadIdx.x; c0 < total; c0 += 8 * blockDim.x) {
+                uint4 v[8];
+                int dst[8];
+#pragma unroll
+                for (int u = 0; u < 8; u++) {
+                    const int c = c0 + u * blockDim.x;
+                    dst[u] = -1;
+                    if (c < total) {
+                        const int tok = c >> 5, part = c & 31, isv = part >> 4, ch = part & 15;
+                        const int j = t0 + tok;
+                        const long long po = s_page[(j >> 4) - p_first];
+                        if (po < 0) {
+                            ok = false;
+                        } else {
+                            v[u] = reinterpret_cast<const uint4 *>((isv ? L.v_pool : L.k_pool) + po +
+                                                                   (size_t)(j & 15) * kD)[ch];
+                            dst[u] = (isv ? kBandTile * kBandRow : 0) + tok * kBandRow + ch * 16;
+                        }
+                    }
                 }
-                const uint4 v = reinterpret_cast<const uint4 *>((isv ? L.v_pool : L.k_pool) + off)[ch];
-                *reinterpret_cast<uint4 *>((isv ? Vs : Ks) + tok * kBandRow + ch * 16) = v;
+#pragma unroll
+                for (int u = 0; u < 8; u++)
+                    if (dst[u] >= 0) *reinterpret_cast<uint4 *>(band_smem + dst[u]) = v[u];
             }
             __syncthreads();
             // scores: lane owns tokens lane and lane+32 of the tile

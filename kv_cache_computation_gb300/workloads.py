@@ -17,7 +17,12 @@ so seeded synthetic streams of the same shapes stand in for them):
   index, both rounded to bf16;
 * pre-RoPE decode queries q~_t: an AR(1) process per (request, head,
   channel), q~_t = rho q~_{t-1} + sqrt(1 - rho^2) eps_t, rounded to bf16 (rho
-  may differ per head), or a forced-hit stream (see ``forced_hit_queries``);
+  may differ per head), or a forced-hit stream (per (request, KV group,
+  step) Bernoulli), or a stream that recurs at a fixed gap (q~_t =
+  q~_{t-gap} + noise), or a topic-revisiting stream (each (request, head)
+  walks a Markov chain over a few prototype directions; q~_t is the current
+  prototype plus noise), whose ``lead`` earliest steps can serve as prefill
+  queries (``prefill_queries``);
 * post-RoPE queries q_t = RoPE(q~_t) at the new token's index, in fp64,
   rounded to bf16;
 * new tokens' K (RoPE'd) and V per step, i.i.d. N(0, 1);
@@ -106,6 +111,12 @@ class DecodeConfig:
     rho_range: Optional[Sequence[float]] = None   # per-head rho ~ U[lo, hi]
     forced_hit_rate: Optional[float] = None        # per (request, kv group, step) Bernoulli
     paged: bool = True
+    gap: Optional[int] = None          # q~_t = q~_{t-gap} + gap_noise eps (fresh N(0,1) before)
+    gap_noise: float = 0.1
+    topics: Optional[int] = None       # prototypes of the topic-revisiting stream
+    topic_stay: float = 0.9            # probability of keeping the current prototype
+    topic_noise: float = 0.1
+    lead: int = 0                      # query-process steps before decode step 0 (prefill queries)
     layers: int = 1
     channel_scale_range: Optional[Sequence[float]] = None   # log-uniform per (layer, kv-head, channel)
     rope_base: float = 500000.0
@@ -205,6 +216,41 @@ def head_rhos(cfg: DecodeConfig, layer: int = 0) -> torch.Tensor:
     return lo + (hi - lo) * torch.rand((cfg.heads,), generator=g, dtype=torch.float64)
 
 
+def _query_process(cfg: DecodeConfig, layer: int, device, total: int):
+    """Pre-RoPE queries (fp64 [total, B, H, d]) of the gap or topic stream,
+    step 0 being the first of the ``lead`` prefill steps."""
+    B, H, d = cfg.batch, cfg.heads, cfg.head_dim
+    out = torch.empty((total, B, H, d), dtype=torch.float64, device=device)
+    if cfg.gap is not None:
+        for t in range(total):
+            eps = randn((B, H, d), derive_seed(cfg.seed, layer, _T_EPS, t), device)
+            out[t] = eps if t < cfg.gap else out[t - cfg.gap] + cfg.gap_noise * eps
+        return out
+    proto = randn((cfg.topics, B, H, d), derive_seed(cfg.seed, layer, _T_Q0), device)
+    g = _gen(derive_seed(cfg.seed, layer, _T_FORCE), device)
+    z = torch.randint(0, cfg.topics, (B, H), generator=g, device=device)
+    bh = torch.arange(B * H, device=device)
+    for t in range(total):
+        if t > 0:
+            move = torch.rand((B, H), generator=g, device=device, dtype=torch.float64) >= cfg.topic_stay
+            z = torch.where(move, torch.randint(0, cfg.topics, (B, H), generator=g, device=device), z)
+        base = proto.permute(1, 2, 0, 3).reshape(B * H, cfg.topics, d)[bh, z.reshape(-1)].reshape(B, H, d)
+        out[t] = base + cfg.topic_noise * randn((B, H, d), derive_seed(cfg.seed, layer, _T_EPS, t), device)
+    return out
+
+
+def prefill_queries(cfg: DecodeConfig, layer: int = 0, device="cpu"):
+    """The ``lead`` queries of the gap / topic stream that precede decode
+    step 0, as prefill queries of tokens context - lead .. context - 1:
+    q_pre, q_post bf16 [lead, B, H, d]."""
+    n, B, H, d = cfg.lead, cfg.batch, cfg.heads, cfg.head_dim
+    q = _query_process(cfg, layer, device, n)
+    q_pre = to_bf16(q)
+    pos = torch.arange(cfg.context - n, cfg.context, device=device)
+    q_post = to_bf16(rope(q_pre.reshape(n, B * H, d), pos, cfg.rope_base).reshape(n, B, H, d))
+    return q_pre, q_post
+
+
 def decode_inputs(cfg: DecodeConfig, layer: int = 0, device="cpu", steps: Optional[int] = None,
                   first_step: int = 0):
     """Per-step inputs for decode steps [first_step, first_step + steps).
@@ -228,8 +274,13 @@ def decode_inputs(cfg: DecodeConfig, layer: int = 0, device="cpu", steps: Option
     rho = head_rhos(cfg, layer).to(device)[None, :, None]
     if cfg.forced_hit_rate is not None:
         gf = _gen(derive_seed(cfg.seed, layer, _T_FORCE), device)
+    proc = None
+    if cfg.gap is not None or cfg.topics is not None:
+        proc = _query_process(cfg, layer, device, cfg.lead + total)
     for t in range(total):
-        if t > 0:
+        if proc is not None:
+            q = proc[cfg.lead + t]
+        elif t > 0:
             eps = randn((B, H, d), derive_seed(cfg.seed, layer, _T_EPS, t), device)
             if cfg.forced_hit_rate is None:
                 q = rho * q + torch.sqrt(1.0 - rho * rho) * eps

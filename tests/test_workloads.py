@@ -103,3 +103,36 @@ def test_named_workloads():
     c4 = W.qwen_moe_stack_120k_b4()
     assert c4.layers == 48 and c4.kv_heads == 4 and c4.context == 122880
     assert c3.kv_bytes_full_per_step(0) == 131073 * 8 * 128 * 4
+
+
+def test_gap_stream_recurs_at_its_gap():
+    """q~_t = q~_{t-gap} + 0.1 eps: the query of `gap` steps back is ~0.1
+    away (relative), the one just before is an unrelated draw."""
+    cfg = _small(gap=4, gap_noise=0.1, heads=4, kv_heads=2, head_dim=64, steps=40)
+    q = W.decode_inputs(cfg)["q_pre"].double()
+    rel = lambda a, b: ((a - b).norm(dim=-1) / a.norm(dim=-1)).mean().item()
+    at_gap = [rel(q[t], q[t - 4]) for t in range(4, 40)]
+    at_one = [rel(q[t], q[t - 1]) for t in range(4, 40)]
+    assert max(at_gap) < 0.15 and min(at_one) > 1.0
+
+
+def test_topic_stream_prefill_queries_lead_into_decode():
+    """The topic stream's `lead` prefill queries are the process steps just
+    before decode step 0: the same process with lead 0 and lead + S steps
+    holds both, in order; queries revisit a few prototypes, so most decode
+    queries have an earlier query within 0.2 (relative) among the previous
+    lead + t ones."""
+    lead, S = 24, 30
+    a = _small(topics=4, topic_stay=0.9, topic_noise=0.05, lead=lead, steps=S, heads=4, kv_heads=2, head_dim=64)
+    b = _small(topics=4, topic_stay=0.9, topic_noise=0.05, lead=0, steps=lead + S, heads=4, kv_heads=2, head_dim=64)
+    qp, qq = W.prefill_queries(a)
+    assert qp.shape == (lead, 2, 4, 64) and qq.shape == qp.shape
+    dec_a = W.decode_inputs(a)["q_pre"]
+    dec_b = W.decode_inputs(b)["q_pre"]
+    assert torch.equal(dec_b[:lead], qp) and torch.equal(dec_b[lead:], dec_a)
+    allq = dec_b.double()
+    near = 0
+    for t in range(lead, lead + S):
+        d = ((allq[:t] - allq[t]).norm(dim=-1) / allq[t].norm(dim=-1)).min(dim=0).values
+        near += (d < 0.2).float().mean().item()
+    assert near / S > 0.8
