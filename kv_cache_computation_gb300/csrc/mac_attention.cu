@@ -676,19 +676,23 @@ __global__ void __launch_bounds__(NW * 32, MINB) attention_kernel(Layout L, Step
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
                 }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                // The reference maximum moves only when a page's scores pass
+                // it by more than kLazyMax (log2 units), so weights stay <= 2^8
+                // and the accumulators are rescaled once or twice per item
+                // rather than on most pages.
+                const float mn0 = mx0 > m0 + kLazyMax ? mx0 : m0, mn1 = mx1 > m1 + kLazyMax ? mx1 : m1;
                 const float bs0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
                 const float bs1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
                 float pr[2][4];
 #pragma unroll
                 for (int j = 0; j < 2; j++) {
-                    pr[j][0] = exp2f(z[j][0] - bs0);
-                    pr[j][1] = exp2f(z[j][1] - bs0);
-                    pr[j][2] = exp2f(z[j][2] - bs1);
-                    pr[j][3] = exp2f(z[j][3] - bs1);
+                    pr[j][0] = ex2_approx(z[j][0] - bs0);
+                    pr[j][1] = ex2_approx(z[j][1] - bs0);
+                    pr[j][2] = ex2_approx(z[j][2] - bs1);
+                    pr[j][3] = ex2_approx(z[j][3] - bs1);
                 }
                 if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-                    const float al0 = exp2f(m0 - bs0), al1 = exp2f(m1 - bs1);
+                    const float al0 = ex2_approx(m0 - bs0), al1 = ex2_approx(m1 - bs1);
                     l0 *= al0;
                     l1 *= al1;
 #pragma unroll

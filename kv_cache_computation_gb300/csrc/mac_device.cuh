@@ -133,6 +133,15 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22, results below 2^-126 flushed to 0; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // log(1 - e^x), x <= 0: Maechler (2012), "Accurately computing
 // log(1 - exp(-|a|))" -- log(-expm1(x)) above -ln 2, log1p(-exp(x)) below.
 __device__ __forceinline__ float log1mexp_f(float x)

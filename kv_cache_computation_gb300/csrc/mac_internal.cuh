@@ -86,6 +86,7 @@ constexpr int kHmWideGroups = MAC_HM_WIDE_GROUPS;
 #define MAC_HM_STAGES_32 3
 #endif
 constexpr int kHmStages32 = MAC_HM_STAGES_32;   // pipeline stages per page lane, 32-head groups
+constexpr float kLazyMax = 8.0f;   // heads-on-M attention: a page moves the softmax reference past this margin
 constexpr float kRemovalMinCond = 1.0f / 32.0f;   // Amend: 1 - e^delta below this -> direct form
 constexpr int kMinChunk = 64;           // smallest work-item span in tokens
 constexpr int kPlanCache = 1024;        // groups the planner caches in shared memory
