@@ -490,6 +490,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) attention_kernel(Layout L, Step
         const int lo_max = max(lo0, lo1);
 
         float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+        float up0 = -CUDART_INF_F, up1 = -CUDART_INF_F;   // HM: raw score above which a row's reference moves
         constexpr int NACC = HM ? 16 : 8;   // O^T m-tiles of 16 dims, or O n-tiles of 8 dims (HM)
         float acc[NACC][4];
 #pragma unroll
@@ -654,11 +655,12 @@ __global__ void __launch_bounds__(NW * 32, MINB) attention_kernel(Layout L, Step
                         mma_bf16(sc[1][kk & 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
                     }
                 }
+                // raw scores (the scale sl2 > 0 is applied inside the exponent)
                 float z[2][4];
 #pragma unroll
                 for (int j = 0; j < 2; j++)
 #pragma unroll
-                    for (int e = 0; e < 4; e++) z[j][e] = (sc[j][0][e] + sc[j][1][e]) * sl2;
+                    for (int e = 0; e < 4; e++) z[j][e] = sc[j][0][e] + sc[j][1][e];
                 if (pg * 16 < lo_max || pg * 16 + 16 > shi) {
 #pragma unroll
                     for (int j = 0; j < 2; j++)
@@ -669,30 +671,21 @@ __global__ void __launch_bounds__(NW * 32, MINB) attention_kernel(Layout L, Step
                             if (!(tok >= lo1 && tok < shi)) z[j][2 + e] = -CUDART_INF_F;
                         }
                 }
+                // The reference maximum of a row moves only when a page's
+                // scores pass it by more than kLazyMax (log2 units), so weights
+                // stay <= 2^8; only then (about once per item) is the row's
+                // maximum reduced over its quad and the accumulators rescaled.
                 float mx0 = fmaxf(fmaxf(z[0][0], z[0][1]), fmaxf(z[1][0], z[1][1]));
                 float mx1 = fmaxf(fmaxf(z[0][2], z[0][3]), fmaxf(z[1][2], z[1][3]));
+                if (__any_sync(0xffffffffu, mx0 > up0 || mx1 > up1)) {
 #pragma unroll
-                for (int o = 1; o < 4; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                }
-                // The reference maximum moves only when a page's scores pass
-                // it by more than kLazyMax (log2 units), so weights stay <= 2^8
-                // and the accumulators are rescaled once or twice per item
-                // rather than on most pages.
-                const float mn0 = mx0 > m0 + kLazyMax ? mx0 : m0, mn1 = mx1 > m1 + kLazyMax ? mx1 : m1;
-                const float bs0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-                const float bs1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-                float pr[2][4];
-#pragma unroll
-                for (int j = 0; j < 2; j++) {
-                    pr[j][0] = ex2_approx(z[j][0] - bs0);
-                    pr[j][1] = ex2_approx(z[j][1] - bs0);
-                    pr[j][2] = ex2_approx(z[j][2] - bs1);
-                    pr[j][3] = ex2_approx(z[j][3] - bs1);
-                }
-                if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-                    const float al0 = ex2_approx(m0 - bs0), al1 = ex2_approx(m1 - bs1);
+                    for (int o = 1; o < 4; o <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                    }
+                    const float mn0 = mx0 > up0 ? mx0 * sl2 : m0, mn1 = mx1 > up1 ? mx1 * sl2 : m1;
+                    const float al0 = ex2_approx(m0 - (mn0 == -CUDART_INF_F ? 0.f : mn0));
+                    const float al1 = ex2_approx(m1 - (mn1 == -CUDART_INF_F ? 0.f : mn1));
                     l0 *= al0;
                     l1 *= al1;
 #pragma unroll
@@ -702,11 +695,22 @@ __global__ void __launch_bounds__(NW * 32, MINB) attention_kernel(Layout L, Step
                         acc[i][2] *= al1;
                         acc[i][3] *= al1;
                     }
+                    m0 = mn0;
+                    m1 = mn1;
+                    up0 = m0 == -CUDART_INF_F ? -CUDART_INF_F : (m0 + kLazyMax) / sl2;
+                    up1 = m1 == -CUDART_INF_F ? -CUDART_INF_F : (m1 + kLazyMax) / sl2;
+                }
+                const float nb0 = m0 == -CUDART_INF_F ? 0.f : -m0, nb1 = m1 == -CUDART_INF_F ? 0.f : -m1;
+                float pr[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; j++) {
+                    pr[j][0] = ex2_approx(fmaf(z[j][0], sl2, nb0));
+                    pr[j][1] = ex2_approx(fmaf(z[j][1], sl2, nb0));
+                    pr[j][2] = ex2_approx(fmaf(z[j][2], sl2, nb1));
+                    pr[j][3] = ex2_approx(fmaf(z[j][3], sl2, nb1));
                 }
                 l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
                 l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-                m0 = mn0;
-                m1 = mn1;
                 // P as the A operand (k = token): a0 rows r4 tokens 2 c4.., a1
                 // row r4 + 8, a2 / a3 the same at tokens 8 + 2 c4..; hi + lo
                 uint32_t ph[4], plo[4];
