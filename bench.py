@@ -120,7 +120,7 @@ def kernel_source_sha(files):
 
 
 KERNEL_SOURCES = [os.path.join(ROOT, "kv_cache_computation_gb300", "csrc", f)
-                  for f in ("mac_attention.cu", "mac_device.cuh", "mac_internal.cuh")]
+                  for f in ("mac_attention.cu", "mac_plan.cuh", "mac_device.cuh", "mac_internal.cuh")]
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_128k.json")

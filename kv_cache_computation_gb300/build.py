@@ -11,8 +11,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmac.so")
-SOURCES = ["mac_api.cu", "mac_kernels.cu", "mac_attention.cu", "mac_noalloc.cu"]
-HEADERS = ["mac_internal.cuh", "mac_device.cuh", os.path.join("..", "..", "include", "mac.h")]
+SOURCES = ["mac_api.cu", "mac_kernels.cu", "mac_attention.cu", "mac_attention_tc.cu", "mac_noalloc.cu"]
+HEADERS = ["mac_internal.cuh", "mac_device.cuh", "mac_plan.cuh", os.path.join("..", "..", "include", "mac.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC"] + ARCH
 

@@ -82,6 +82,18 @@ constexpr int kHmMinCtas16 = MAC_HM_MIN_CTAS_16;
 constexpr int kHmMinCtas32 = MAC_HM_MIN_CTAS_32;
 constexpr int kHmMinCtas32Wide = MAC_HM_MIN_CTAS_32_WIDE;
 constexpr int kHmWideGroups = MAC_HM_WIDE_GROUPS;
+// 1: 32-head groups stream through the tcgen05 kernel (mac_attention_tc.cu;
+// blocks of 64 tokens, kTcStages of them in flight per CTA) instead of the
+// mma.sync heads-on-M kernel.  A comparison build for now: one block at a
+// time per SM, it is slower than the mma.sync form.
+#ifndef MAC_ATTN_TC32
+#define MAC_ATTN_TC32 0
+#endif
+#ifndef MAC_TC_STAGES
+#define MAC_TC_STAGES 4
+#endif
+constexpr bool kTc32 = MAC_ATTN_TC32 != 0;
+constexpr int kTcStages = MAC_TC_STAGES;
 #ifndef MAC_HM_STAGES_32
 #define MAC_HM_STAGES_32 3
 #endif
@@ -94,7 +106,7 @@ constexpr int kBandTile = 64;           // tokens per shared-memory tile of the 
 constexpr int kBandRow = 272;           // padded bytes per staged K/V row (conflict-free per-lane rows)
 
 // device error bits
-enum : uint32_t { kErrPage = 1u, kErrSlot = 2u, kErrPos = 4u };
+enum : uint32_t { kErrPage = 1u, kErrSlot = 2u, kErrPos = 4u, kErrTimeout = 8u };
 
 // device counters
 enum { kStSteps = 0, kStDecisions, kStHits, kStKvRead, kStKvFull, kStDirect, kStItems, kStCount };
@@ -180,6 +192,8 @@ cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_append(const Layout &L, int req, int start, int n, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, cudaStream_t s);
 cudaError_t attention_kernel_config(int G, bool wide, size_t *smem, int *ctas_per_sm);
+cudaError_t attention_tc_config(size_t *smem, int *ctas_per_sm);                        // mac_attention_tc.cu
+cudaError_t launch_attention_tc(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s);
 bool attention_wide(int G, int groups);   // whether a step of `groups` groups takes the wide variant
 cudaError_t amend_kernel_config();
 
