@@ -105,6 +105,10 @@ typedef struct {
     uint64_t work_items;      /* attention work items planned                   */
     uint32_t device_error;    /* bounds-check bits (0 = none)                   */
     uint32_t reserved;
+    uint64_t tcgen05_steps;   /* of the steps, those whose attention ran on the */
+                              /* tcgen05 kernel (groups of 32 heads, steps of   */
+                              /* at least 32768 KV tokens); the others ran on   */
+                              /* the mma.sync kernel                            */
 } mac_stats;
 
 /* Accumulated GPU time per phase since profiling was enabled (ms). */

@@ -32,7 +32,8 @@ class MacStats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_uint64), ("head_decisions", ctypes.c_uint64), ("hits", ctypes.c_uint64),
                 ("kv_tokens_read", ctypes.c_uint64), ("kv_tokens_full", ctypes.c_uint64),
                 ("removal_direct", ctypes.c_uint64), ("work_items", ctypes.c_uint64),
-                ("device_error", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+                ("device_error", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("tcgen05_steps", ctypes.c_uint64)]
 
 
 class MacProfile(ctypes.Structure):

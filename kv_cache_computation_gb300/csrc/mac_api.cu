@@ -139,6 +139,10 @@ struct mac_ctx {
     int grid_ctas = 0;
     int grid_ctas_wide = 0;   // grid of the attention variant for steps of many groups (0: none)
     size_t attn_smem = 0;
+    int grid_ctas_tc = 0;     // grid of the tcgen05 attention kernel (0: not available)
+    uint64_t tc_steps = 0;    // steps whose attention ran on it
+    TcMaps tc_maps{};         // its TMA descriptors of the two pools
+    size_t attn_smem_tc = 0;
     cudaStream_t side = nullptr;
     cudaEvent_t ev_complete = nullptr, ev_amend = nullptr;
     bool amend_pending = false;
@@ -294,8 +298,12 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
     a.lse_out = lse_out;
     a.force = (!full && h->force_next) ? 1 : 0;
     a.full_mode = full ? 1 : 0;
-    a.wide = (h->grid_ctas_wide > 0 && attention_wide(h->lay.G, batch * h->lay.Hkv)) ? 1 : 0;
-    a.grid_ctas = a.wide ? h->grid_ctas_wide : h->grid_ctas;
+    long long tokens = 0;   // KV tokens the step holds, all requests and KV heads
+    for (int b = 0; b < batch; b++) tokens += h->kv_len[b] + 1;
+    tokens *= h->lay.Hkv;
+    a.tc = (h->grid_ctas_tc > 0 && tokens >= kTcMinTokens) ? 1 : 0;
+    a.wide = (!a.tc && h->grid_ctas_wide > 0 && attention_wide(h->lay.G, batch * h->lay.Hkv)) ? 1 : 0;
+    a.grid_ctas = a.tc ? h->grid_ctas_tc : (a.wide ? h->grid_ctas_wide : h->grid_ctas);
     a.plan_mode = h->cfg.plan_mode;
     h->force_next = false;
 
@@ -323,7 +331,7 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
         // from the device copy Match keeps (q_stash, same layout)
         StepArgs aa = a;
         if (host_io) aa.q_post = h->lay.q_stash;
-        MAC_CUDA(h, launch_attention(h->lay, aa, h->attn_smem, s));
+        MAC_CUDA(h, launch_attention(h->lay, aa, &h->tc_maps, a.tc ? h->attn_smem_tc : h->attn_smem, s));
     }
     if (pe) MAC_CUDA(h, cudaEventRecord(pe[2], s));
     MAC_CUDA(h, launch_combine(h->lay, a, s));
@@ -346,6 +354,7 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
         h->kv_len[b] += 1;
         if (!full) h->steps[b] += 1;
     }
+    h->tc_steps += a.tc ? 1 : 0;
     return MAC_OK;
 }
 
@@ -417,14 +426,31 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     e = cudaGetDeviceProperties(&prop, h->device);
     if (e != cudaSuccess) return fail(e, "cudaGetDeviceProperties");
     if (prop.major * 10 + prop.minor != 103) return fail(cudaErrorNoKernelImageForDevice, "device check (sm_103a required)");
+    // 32-head groups: the tcgen05 kernel needs TMA descriptors of the two
+    // pools; if they cannot be made, the mma.sync kernel serves every step
+    Layout &L = h->lay;
     int per_sm = 0;
-    e = attention_kernel_config(z.G, false, &h->attn_smem, &per_sm);
+    if (attention_tc_wanted(z.G)) {
+        char *kvp = (char *)dev_kv;
+        L.k_pool = (__nv_bfloat16 *)kvp;
+        L.v_pool = (__nv_bfloat16 *)(kvp + align_up(z.kv_each));
+        size_t smem_tc = 0;
+        if (attention_tc_maps(L, h->tc_maps, (int64_t)(z.kv_each / (kD * 2))) == cudaSuccess &&
+            attention_kernel_config(z.G, false, true, &smem_tc, &per_sm) == cudaSuccess && per_sm >= 1) {
+            h->attn_smem_tc = smem_tc;
+            h->grid_ctas_tc = std::min(prop.multiProcessorCount * per_sm, kMaxCtas);
+        } else {
+            L.tc = 0;
+        }
+        cudaGetLastError();
+    }
+    e = attention_kernel_config(z.G, false, false, &h->attn_smem, &per_sm);
     if (e != cudaSuccess) return fail(e, "attention kernel configuration");
     if (per_sm < 1) return fail(cudaErrorInvalidConfiguration, "attention kernel occupancy");
     h->grid_ctas = std::min(prop.multiProcessorCount * per_sm, kMaxCtas);
     if (attention_wide(z.G, kMaxGroupsPerStep)) {
         size_t smem_w = 0;
-        e = attention_kernel_config(z.G, true, &smem_w, &per_sm);
+        e = attention_kernel_config(z.G, true, false, &smem_w, &per_sm);
         if (e != cudaSuccess) return fail(e, "attention kernel configuration");
         if (per_sm < 1 || smem_w != h->attn_smem) return fail(cudaErrorInvalidConfiguration, "attention kernel occupancy");
         h->grid_ctas_wide = std::min(prop.multiProcessorCount * per_sm, kMaxCtas);
@@ -433,7 +459,6 @@ mac_status mac_create(const mac_config *cfg, void *dev_kv, size_t kv_bytes, void
     if (e != cudaSuccess) return fail(e, "amend kernel configuration");
 
     char *kv = (char *)dev_kv, *rg = (char *)dev_ring, *sc = (char *)dev_scratch;
-    Layout &L = h->lay;
     L.H = cfg->heads;
     L.Hkv = cfg->kv_heads;
     L.G = z.G;
@@ -663,6 +688,7 @@ mac_status mac_get_stats(mac_handle h, mac_stats *out)
     out->removal_direct = v[kStDirect];
     out->work_items = v[kStItems];
     out->device_error = err;
+    out->tcgen05_steps = h->tc_steps;
     return MAC_OK;
 }
 
@@ -672,6 +698,7 @@ mac_status mac_reset_stats(mac_handle h)
     if (st != MAC_OK) return st;
     MAC_CUDA(h, cudaDeviceSynchronize());
     MAC_CUDA(h, cudaMemset(h->lay.stats, 0, kStCount * 8));
+    h->tc_steps = 0;
     return MAC_OK;
 }
 

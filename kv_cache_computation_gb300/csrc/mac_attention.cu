@@ -697,15 +697,13 @@ static cudaError_t attention_config_nh(size_t smem, int *ctas_per_sm)
 
 // 32-head groups go to the tcgen05 kernel unless it is switched off
 static bool tensor_memory_path(int G) { return kTc32 && !kAttnCudaCore && G == 32; }
+bool attention_tc_wanted(int G) { return tensor_memory_path(G); }
 
-bool attention_wide(int G, int groups)
-{
-    return !tensor_memory_path(G) && heads_on_m(G) && G == 32 && groups >= kHmWideGroups;
-}
+bool attention_wide(int G, int groups) { return heads_on_m(G) && G == 32 && groups >= kHmWideGroups; }
 
-cudaError_t attention_kernel_config(int G, bool wide, size_t *smem, int *ctas_per_sm)
+cudaError_t attention_kernel_config(int G, bool wide, bool tc, size_t *smem, int *ctas_per_sm)
 {
-    if (tensor_memory_path(G)) return attention_tc_config(smem, ctas_per_sm);
+    if (tc && tensor_memory_path(G)) return attention_tc_config(smem, ctas_per_sm);
     *smem = attention_smem(G);
     if (heads_on_m(G)) {
         if (G == 16) return attention_config_nh<1, true, kAttnStages, kHmMinCtas16>(*smem, ctas_per_sm);
@@ -719,9 +717,9 @@ cudaError_t attention_kernel_config(int G, bool wide, size_t *smem, int *ctas_pe
     }
 }
 
-cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s)
+cudaError_t launch_attention(const Layout &L, const StepArgs &a, const TcMaps *maps, size_t smem, cudaStream_t s)
 {
-    if (tensor_memory_path(L.G)) return launch_attention_tc(L, a, smem, s);
+    if (a.tc && tensor_memory_path(L.G) && L.tc && maps) return launch_attention_tc(L, a, *maps, smem, s);
     const dim3 grid(a.grid_ctas), block(kAttnWarps * 32);
     if (heads_on_m(L.G)) {
         if (L.G == 16)

@@ -249,9 +249,9 @@ __device__ __forceinline__ void dot8_bf16(float &acc, uint4 a, uint4 b)
 
 }  // namespace
 
-template <typename Kernel>
+template <typename Kernel, typename... Args>
 static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                                    const Layout &L, const StepArgs &a)
+                                    const Args &...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -263,7 +263,7 @@ static cudaError_t launch_maybe_pdl(Kernel k, dim3 grid, dim3 block, size_t smem
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k, L, a);
+    return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 }  // namespace macgpu

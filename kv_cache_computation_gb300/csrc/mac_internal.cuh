@@ -3,6 +3,7 @@
 // public ABI (include/mac.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -82,18 +83,26 @@ constexpr int kHmMinCtas16 = MAC_HM_MIN_CTAS_16;
 constexpr int kHmMinCtas32 = MAC_HM_MIN_CTAS_32;
 constexpr int kHmMinCtas32Wide = MAC_HM_MIN_CTAS_32_WIDE;
 constexpr int kHmWideGroups = MAC_HM_WIDE_GROUPS;
-// 1: 32-head groups stream through the tcgen05 kernel (mac_attention_tc.cu;
-// blocks of 64 tokens, kTcStages of them in flight per CTA) instead of the
-// mma.sync heads-on-M kernel.  A comparison build for now: one block at a
-// time per SM, it is slower than the mma.sync form.
+// 1: steps of 32-head groups that hold at least MAC_TC_MIN_TOKENS KV tokens
+// (over all requests and KV heads) stream through the tcgen05 kernel
+// (mac_attention_tc.cu; blocks of 128 tokens, key and value rings of
+// MAC_TC_K_STAGES and MAC_TC_V_STAGES blocks); smaller steps, whose time is
+// mostly the kernels' fixed costs, keep the mma.sync heads-on-M kernel.
+// 0: the mma.sync kernel for every step (comparison build).
 #ifndef MAC_ATTN_TC32
-#define MAC_ATTN_TC32 0
+#define MAC_ATTN_TC32 1
 #endif
-#ifndef MAC_TC_STAGES
-#define MAC_TC_STAGES 4
+#ifndef MAC_TC_MIN_TOKENS
+#define MAC_TC_MIN_TOKENS 32768
+#endif
+constexpr long long kTcMinTokens = MAC_TC_MIN_TOKENS;
+#ifndef MAC_TC_K_STAGES
+#define MAC_TC_K_STAGES 2
+#endif
+#ifndef MAC_TC_V_STAGES
+#define MAC_TC_V_STAGES 3
 #endif
 constexpr bool kTc32 = MAC_ATTN_TC32 != 0;
-constexpr int kTcStages = MAC_TC_STAGES;
 #ifndef MAC_HM_STAGES_32
 #define MAC_HM_STAGES_32 3
 #endif
@@ -121,6 +130,7 @@ struct Layout {
     int ctx_stride;           // contiguous: tokens reserved per (request, kv-head)
     int item_cap;
     int amend_band;           // 0: reuse Complete's band summary; 1: recompute it in Amend
+    int tc;                   // the pools' TMA descriptors are made: the tcgen05 attention kernel can serve
     float tau2;               // tau^2 (fp32)
     float scale_log2;         // sm_scale * log2(e)
 
@@ -169,6 +179,12 @@ struct Layout {
                     // and Combine sets the word back to INT_MAX for the next step
 };
 
+// TMA descriptors of the K and V pools (rows of 128 bf16; box 16 rows x 64
+// columns, 128-byte swizzle), a parameter of the tcgen05 attention kernel only.
+struct TcMaps {
+    CUtensorMap kmap, vmap;
+};
+
 struct StepArgs {
     int batch;
     const __nv_bfloat16 *q_pre, *q_post, *k_new, *v_new;
@@ -180,20 +196,23 @@ struct StepArgs {
     int plan_mode;    // 0 balanced, 1 equal split per group
     int pdl;          // launch attention / combine as programmatic dependents
     int wide;         // attention: the variant for many groups (grid_ctas is its grid)
+    int tc;           // attention: the tcgen05 kernel (grid_ctas is its grid)
 };
 
 // launchers (mac_kernels.cu)
 cudaError_t launch_match_plan(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_seed(const Layout &L, int req, int first, int n, int base_step, const __nv_bfloat16 *q,
                         const float *o, const float *lse, cudaStream_t s);
-cudaError_t launch_attention(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s);
+cudaError_t launch_attention(const Layout &L, const StepArgs &a, const TcMaps *maps, size_t smem, cudaStream_t s);
 cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_amend(const Layout &L, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_append(const Layout &L, int req, int start, int n, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, cudaStream_t s);
-cudaError_t attention_kernel_config(int G, bool wide, size_t *smem, int *ctas_per_sm);
+cudaError_t attention_kernel_config(int G, bool wide, bool tc, size_t *smem, int *ctas_per_sm);
+bool attention_tc_wanted(int G);                                                        // mac_attention.cu
 cudaError_t attention_tc_config(size_t *smem, int *ctas_per_sm);                        // mac_attention_tc.cu
-cudaError_t launch_attention_tc(const Layout &L, const StepArgs &a, size_t smem, cudaStream_t s);
+cudaError_t attention_tc_maps(Layout &L, TcMaps &maps, int64_t pool_rows);              // mac_attention_tc.cu
+cudaError_t launch_attention_tc(const Layout &L, const StepArgs &a, const TcMaps &maps, size_t smem, cudaStream_t s);
 bool attention_wide(int G, int groups);   // whether a step of `groups` groups takes the wide variant
 cudaError_t amend_kernel_config();
 

@@ -128,7 +128,7 @@ mac_status setup_device(int dev, DeviceSetup **out)
         const int groups[6] = {1, 2, 4, 8, 16, 32};
         for (int i = 0; i < 6; i++) {
             int per_sm = 0;
-            if (attention_kernel_config(groups[i], false, &s.smem[i], &per_sm) != cudaSuccess || per_sm < 1)
+            if (attention_kernel_config(groups[i], false, false, &s.smem[i], &per_sm) != cudaSuccess || per_sm < 1)
                 return MAC_ERR_CUDA;
             s.ctas[i] = s.sm_count * per_sm < kMaxCtas ? s.sm_count * per_sm : kMaxCtas;
         }
@@ -215,7 +215,7 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
     if (cudaMemsetAsync(sc + c.stats, 0, c.err + 4 - c.stats, cs) != cudaSuccess) return MAC_ERR_CUDA;
     noalloc_prepare_kernel<<<1, 256, 0, cs>>>(L, pa);
     if (cudaGetLastError() != cudaSuccess) return MAC_ERR_CUDA;
-    if (launch_attention(L, a, s->smem[gi], cs) != cudaSuccess) return MAC_ERR_CUDA;
+    if (launch_attention(L, a, nullptr, s->smem[gi], cs) != cudaSuccess) return MAC_ERR_CUDA;
     if (launch_combine(L, a, cs) != cudaSuccess) return MAC_ERR_CUDA;
     return MAC_OK;
 }

@@ -132,3 +132,23 @@ def test_host_binding_refuses_what_the_kernels_cannot_address():
             _host(p, "q_pre", torch.float32)
         with pytest.raises(ValueError):
             _host(p, "q_pre", torch.bfloat16, (2, 4, 64))
+
+
+def _struct_fields(name):
+    """(type, field) pairs of the typedef struct `name` in include/mac.h."""
+    src = open(os.path.join(ROOT, "include", "mac.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    body = re.search(r"typedef struct\s*\{([^}]*)\}\s*" + name + r"\s*;", src).group(1)
+    return re.findall(r"\b(u?int\d+_t|int|float|double)\s+(\w+)\s*;", body)
+
+
+@pytest.mark.parametrize("cname,pyname", [("mac_config", "MacConfig"), ("mac_stats", "MacStats"),
+                                          ("mac_profile", "MacProfile")])
+def test_binding_structs_match_the_header(native, cname, pyname):
+    """The ctypes structures the binding passes to the library declare the
+    header's fields in the header's order with the header's widths."""
+    width = {"int": 4, "float": 4, "double": 8, "int32_t": 4, "uint32_t": 4, "int64_t": 8, "uint64_t": 8}
+    hdr = _struct_fields(cname)
+    py = getattr(native, pyname)._fields_
+    assert [f for _, f in hdr] == [f for f, _ in py]
+    assert [width[t] for t, _ in hdr] == [ctypes.sizeof(t) for _, t in py]
