@@ -304,6 +304,7 @@ mac_status run_step(mac_ctx *h, int batch, const void *q_pre, const void *q_post
     a.tc = (h->grid_ctas_tc > 0 && tokens >= kTcMinTokens) ? 1 : 0;
     a.wide = (!a.tc && h->grid_ctas_wide > 0 && attention_wide(h->lay.G, batch * h->lay.Hkv)) ? 1 : 0;
     a.grid_ctas = a.tc ? h->grid_ctas_tc : (a.wide ? h->grid_ctas_wide : h->grid_ctas);
+    a.plan_ctas = (a.tc && tokens >= kTcWaveTokens * a.grid_ctas) ? kTcPlanWaves * a.grid_ctas : a.grid_ctas;
     a.plan_mode = h->cfg.plan_mode;
     h->force_next = false;
 

@@ -154,7 +154,10 @@ __device__ __forceinline__ void mbar_wait_bounded(uint32_t mbar, uint32_t parity
         if (mbar_test(mbar, parity)) return;
 }
 
-// Bounded wait that also gives up once another role has failed.
+// Bounded wait that also gives up once another role has failed.  The lanes
+// of a warp run it in step on the same barrier word and the same flag, so
+// they leave it together with the same verdict before any warp-wide
+// instruction that follows.
 __device__ __forceinline__ bool mbar_wait_or_fail(uint32_t mbar, uint32_t parity, volatile int *fail)
 {
     for (uint32_t i = 0; i < kTcSpinLimit; i++) {
@@ -483,22 +486,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
         // softmax: thread (t, half) holds token t of each block for the heads
         // h0 .. h0 + 15
         const int t = tid & (kTcTok - 1), h0 = (warp >> 2) * kTcHalf;
+        // Q of an item (thread: chunks tid and tid + 256 of the 32 x 16) and
+        // its heads' first tokens, fetched one item ahead into registers and
+        // stored as soon as the previous item's score products are done
+        uint4 qn[2];
+        int lon = 0;
+        auto fetch_q = [&](const ItemView &w) {
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                const int i = tid + r * kTcSoftmaxWarps * 32, h = i >> 4, c = i & 15;
+                qn[r] = reinterpret_cast<const uint4 *>(a.q_post + (w.hrow + h) * kD)[c];
+            }
+            if (tid < kTcHeads) lon = max(max(w.slo, w.ilo), L.dec_lo[w.hrow + tid]);
+        };
+        auto store_q = [&]() {
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                const int i = tid + r * kTcSoftmaxWarps * 32, h = i >> 4, c = i & 15;
+                *reinterpret_cast<uint4 *>(sQ + sw128(kTcHeads, h, c)) = qn[r];
+            }
+            if (tid < kTcHeads) s_lo[tid] = lon;
+            fence_async_smem();
+            mbar_arrive(B_(bar_qfull));
+        };
+        if (blockIdx.x < n_items) {
+            fetch_q(view(blockIdx.x));
+            store_q();
+        }
         uint32_t jbase = 0;
         bool ok = true;
         int k = 0;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, k++) {
             const ItemView v = view(it);
-            // Q and the heads' first tokens (the previous item's score products
-            // are done: their S^T has been read)
-            for (int i = tid; i < kTcHeads * 16; i += kTcSoftmaxWarps * 32) {
-                const int h = i >> 4, c = i & 15;
-                const uint4 q = reinterpret_cast<const uint4 *>(a.q_post + (v.hrow + h) * kD)[c];
-                *reinterpret_cast<uint4 *>(sQ + sw128(kTcHeads, h, c)) = q;
-            }
-            if (tid < kTcHeads) s_lo[tid] = max(max(v.slo, v.ilo), L.dec_lo[v.hrow + tid]);
-            fence_async_smem();
-            mbar_arrive(B_(bar_qfull));
             if (!mbar_wait_or_fail(B_(bar_qfull), k & 1, fail)) break;
+            const bool has_next = it + (int)gridDim.x < n_items;
+            if (has_next) fetch_q(view(it + gridDim.x));
             float m[kTcHalf], l[kTcHalf];   // reference (log2 units), this thread's sum of P, per head
 #pragma unroll
             for (int h = 0; h < kTcHalf; h++) {
@@ -607,6 +629,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                 mbar_arrive(B_(bar_pfull[pb]));
             }
             if (!ok) break;
+            // every score product of the item is done (its S^T has been read):
+            // the next item's Q goes in while this one merges
+            if (has_next) store_q();
             // merge: the item's last P V done, O^T holds the hi and lo products
             const uint32_t last = jbase + v.nblk - 1;
             if (!mbar_wait_or_fail(B_(bar_pempty[last & 1]), (last >> 1) & 1, fail)) break;

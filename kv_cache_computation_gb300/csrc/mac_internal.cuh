@@ -96,6 +96,17 @@ constexpr int kHmWideGroups = MAC_HM_WIDE_GROUPS;
 #define MAC_TC_MIN_TOKENS 32768
 #endif
 constexpr long long kTcMinTokens = MAC_TC_MIN_TOKENS;
+// Steps of at least MAC_TC_WAVE_TOKENS KV tokens per tcgen05 CTA are planned
+// for MAC_TC_PLAN_WAVES items per CTA (the CTA overlaps consecutive items):
+// when the groups do not divide the grid, items of one wave leave CTAs idle.
+#ifndef MAC_TC_PLAN_WAVES
+#define MAC_TC_PLAN_WAVES 2
+#endif
+#ifndef MAC_TC_WAVE_TOKENS
+#define MAC_TC_WAVE_TOKENS 16384
+#endif
+constexpr int kTcPlanWaves = MAC_TC_PLAN_WAVES;
+constexpr long long kTcWaveTokens = MAC_TC_WAVE_TOKENS;
 #ifndef MAC_TC_K_STAGES
 #define MAC_TC_K_STAGES 2
 #endif
@@ -193,6 +204,8 @@ struct StepArgs {
     int force;        // use forced_slot instead of the Match decision
     int full_mode;    // full attention, no Match / Amend
     int grid_ctas;    // attention CTAs
+    int plan_ctas;    // work slots the plan fills: grid_ctas, or a multiple of it for a kernel
+                      // whose CTAs overlap consecutive items
     int plan_mode;    // 0 balanced, 1 equal split per group
     int pdl;          // launch attention / combine as programmatic dependents
     int wide;         // attention: the variant for many groups (grid_ctas is its grid)

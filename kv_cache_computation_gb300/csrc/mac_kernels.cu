@@ -747,9 +747,9 @@ cudaError_t launch_seed(const Layout &L, int req, int first, int n, int base_ste
 
 cudaError_t launch_combine(const Layout &L, const StepArgs &a, cudaStream_t s)
 {
-    // a group holds at most about grid / groups + 2 items
+    // a group holds at most about plan slots / groups + 2 items
     const int nbg = a.batch * L.Hkv;
-    const int per_group = (a.grid_ctas + nbg - 1) / nbg + 2;
+    const int per_group = (a.plan_ctas + nbg - 1) / nbg + 2;
     const dim3 grid(a.batch * L.H);
     // A few items per head (many requests): small blocks, so that the whole
     // grid is resident beside the attention CTAs when their wait releases.

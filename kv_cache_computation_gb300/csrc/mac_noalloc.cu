@@ -207,6 +207,7 @@ extern "C" mac_status mac_attention_noalloc(int batch, int heads, int kv_heads, 
     a.lse_out = dev_lse;
     a.full_mode = 1;
     a.grid_ctas = grid;
+    a.plan_ctas = grid;
     a.plan_mode = 0;
     a.pdl = 0;
 

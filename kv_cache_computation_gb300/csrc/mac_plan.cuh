@@ -63,7 +63,7 @@ __device__ __forceinline__ int plan_chunk(const Layout &L, const StepArgs &a, co
                                           int hi)
 {
     if (a.plan_mode == 0) return ps.C;
-    const int splits = a.grid_ctas / nbg > 1 ? a.grid_ctas / nbg : 1;
+    const int splits = a.plan_ctas / nbg > 1 ? a.plan_ctas / nbg : 1;
     return max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
 }
 
@@ -97,7 +97,7 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
     int C = kMinChunk;
     ChunkDiv RC = {0u, 0};
     if (a.plan_mode == 0) {
-        const int P = a.grid_ctas;
+        const int P = a.plan_ctas;
         int Q = (4 * nseg <= P) ? P : P * (1 + (2 * nseg + P - 1) / P);
         if (Q == P && band_wave_fit(nb, TL, P, L.band_r)) Q = P - nb;
         if (Q > L.item_cap - nb) Q = L.item_cap - nb;
@@ -207,7 +207,7 @@ __device__ void cta_plan(const Layout &L, const StepArgs &a, PlanShared &ps)
                 }
                 return warp_sum_int(c);
             };
-            const long long P = a.grid_ctas;
+            const long long P = a.plan_ctas;
             long long Q = (4ll * nseg <= P) ? P : P * (1 + (2ll * nseg + P - 1) / P);
             if (Q == P && band_wave_fit(nb, TL, (int)P, L.band_r)) Q = P - nb;
             if (Q > L.item_cap - nb) Q = L.item_cap - nb;
