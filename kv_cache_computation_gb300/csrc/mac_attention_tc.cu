@@ -545,10 +545,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                 const bool edge = tok < lo_max || tok >= v.ihi;
                 uint32_t mv = 0;   // heads whose reference this token passes by more than kLazyMax
 #pragma unroll
-                for (int h = 0; h < kTcHalf; h++) {
-                    y[h] = (edge && !(tok >= s_lo[h0 + h] && tok < v.ihi)) ? -CUDART_INF_F : y[h] * sl2;
-                    if (y[h] - m[h] > kLazyMax) mv |= 1u << h;
+                for (int h = 0; h < kTcHalf; h++) y[h] *= sl2;
+                if (edge) {   // a token before a head's first or past the item's last
+#pragma unroll
+                    for (int h = 0; h < kTcHalf; h++)
+                        if (!(tok >= s_lo[h0 + h] && tok < v.ihi)) y[h] = -CUDART_INF_F;
                 }
+#pragma unroll
+                for (int h = 0; h < kTcHalf; h++)
+                    if (y[h] - m[h] > kLazyMax) mv |= 1u << h;
                 const uint32_t wmv = __reduce_or_sync(0xffffffffu, mv);
                 if (wmv) {
 #pragma unroll
