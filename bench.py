@@ -327,7 +327,7 @@ def attention_bytes(st, B, H, G):
     return st["kv_tokens_read"] * BYTES_PER_KV_TOKEN + st["steps"] * B * H * 256 + st["work_items"] * G * (128 * 4 + 8)
 
 
-def method_points(dev, peak, specs, steps=48, warm=4, prof_steps=16, eager=False, on_point=None):
+def method_points(dev, peak, specs, steps=48, warm=4, prof_steps=16, eager=False, on_point=None, plan_mode=0):
     """The MAC step against the in-build full split-KV step (mac_full_step)
     on forced-hit workloads (one handle per (kv_heads, batch, context), the
     same prefill and inputs for both): us/step, KV bytes read vs full, head
@@ -344,7 +344,7 @@ def method_points(dev, peak, specs, steps=48, warm=4, prof_steps=16, eager=False
         H, G = base.heads, base.group
         max_ctx = ctx + n_all + 2
         mac = MacAttention(H, kv, 128, base.ring_len, base.band_r, base.tau, max_batch=B, max_ctx=max_ctx,
-                           page_size=16)
+                           page_size=16, plan_mode=plan_mode)
         pt = W.page_tables(B, (max_ctx + 15) // 16, seed=base.seed).to(dev)
         for b in range(B):
             mac.set_page_table(b, pt[b].contiguous())
@@ -842,10 +842,10 @@ def bench_sweep(args, ws, rank, local):
 
     def emit(pt):
         if rank == 0:
-            print(json.dumps({"workload": "forced_hit_sweep", **pt}), flush=True)
+            print(json.dumps({"workload": "forced_hit_sweep", "plan_mode": args.plan_mode, **pt}), flush=True)
 
     method_points(dev, peak, specs, steps=args.steps, warm=args.warmup, prof_steps=min(16, args.steps),
-                  eager=args.eager, on_point=emit)
+                  eager=args.eager, on_point=emit, plan_mode=args.plan_mode)
     return None
 
 
