@@ -103,7 +103,16 @@ typedef struct {
     uint64_t removal_direct;  /* Amend removals too ill-conditioned for fp32    */
                               /* (1 - e^delta < 1/32), formed directly instead  */
     uint64_t work_items;      /* attention work items planned                   */
-    uint32_t device_error;    /* bounds-check bits (0 = none)                   */
+    uint32_t device_error;    /* bounds-check bits (0 = none; any set makes     */
+                              /* mac_sync return MAC_ERR_STATE and the handle   */
+                              /* sticky): 1 a page-table entry outside          */
+                              /* the pool or a page past the table (its tokens  */
+                              /* are not read; the request's output is then     */
+                              /* wrong, other requests' are not touched); 2 a   */
+                              /* forced slot that holds no entry (taken as a    */
+                              /* miss); 4 more work                             */
+                              /* items than the scratch holds; 8 a wait in the  */
+                              /* tcgen05 kernel gave up (its CTA stopped early) */
     uint32_t reserved;
     uint64_t tcgen05_steps;   /* of the steps, those whose attention ran on the */
                               /* tcgen05 kernel (groups of 32 heads, steps of   */

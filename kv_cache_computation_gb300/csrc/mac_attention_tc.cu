@@ -37,8 +37,12 @@ namespace {
 
 constexpr int kTcTok = 128;                        // tokens per block (8 pages): the M of the score product
 constexpr int kTcHeads = 32;                       // query heads of the group: the N of the score product
-constexpr int kTcSoftmaxWarps = 8;                 // warp w: TMEM lanes 32 (w mod 4) .., heads 16 (w / 4) ..
-constexpr int kTcHalf = 16;                        // heads per softmax thread
+#ifndef MAC_TC_SOFTMAX_WARPS
+#define MAC_TC_SOFTMAX_WARPS 8
+#endif
+constexpr int kTcSoftmaxWarps = MAC_TC_SOFTMAX_WARPS;   // warp w: TMEM lanes 32 (w mod 4) .., heads kTcHalf (w / 4) ..
+constexpr int kTcHalf = kTcHeads * 4 / kTcSoftmaxWarps; // heads per softmax thread (8 or 16)
+static_assert(kTcHalf == 8 || kTcHalf == 16, "8 or 16 softmax warps");
 constexpr int kTcKStages = MAC_TC_K_STAGES;        // key blocks in the ring
 constexpr int kTcVStages = MAC_TC_V_STAGES;        // value blocks in the ring
 constexpr int kTcKWarp = kTcSoftmaxWarps, kTcVWarp = kTcKWarp + 1, kTcMmaWarp = kTcVWarp + 1;
@@ -84,35 +88,6 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void mbar_init(uint32_t mbar, int count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" :: "r"(mbar), "r"(count) : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns of tensor memory, one lane per thread
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
-{
-    uint32_t r[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 lanes x 32 consecutive 32-bit columns of tensor memory, one lane per thread
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
-{
-    uint32_t r[32];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-                   "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar)
@@ -181,16 +156,45 @@ __device__ __forceinline__ uint32_t sw128(int rows, int t, int c)
     return (uint32_t)((c >> 3) * rows * 128 + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+// 32 lanes x N (8 or 16) consecutive 32-bit columns of tensor memory, one
+// lane per thread; the load waits for its data, the store for its completion
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N])
 {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
-                 :: "r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-                    "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-                    "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-                    "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-                    "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-                    "r"(__float_as_uint(v[15]))
-                 : "memory");
+    static_assert(N == 8 || N == 16, "8 or 16 columns");
+    uint32_t r[N];
+    if constexpr (N == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr));
+    } else {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                       "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                     : "r"(taddr));
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; i++) v[i] = __uint_as_float(r[i]);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[N])
+{
+    static_assert(N == 8 || N == 16, "8 or 16 columns");
+    uint32_t r[N];
+#pragma unroll
+    for (int i = 0; i < N; i++) r[i] = __float_as_uint(v[i]);
+    if constexpr (N == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n"
+                     :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+                     :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                     : "memory");
+    }
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
@@ -486,14 +490,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
         // softmax: thread (t, half) holds token t of each block for the heads
         // h0 .. h0 + 15
         const int t = tid & (kTcTok - 1), h0 = (warp >> 2) * kTcHalf;
-        // Q of an item (thread: chunks tid and tid + 256 of the 32 x 16) and
-        // its heads' first tokens, fetched one item ahead into registers and
-        // stored as soon as the previous item's score products are done
-        uint4 qn[2];
+        // Q of an item (thread: chunks tid, tid + 32 x kTcSoftmaxWarps, ... of
+        // the 32 x 16) and its heads' first tokens, fetched one item ahead into
+        // registers and stored as soon as the previous item's score products
+        // are done
+        constexpr int kQPer = kTcHeads * 16 / (kTcSoftmaxWarps * 32);
+        uint4 qn[kQPer];
         int lon = 0;
         auto fetch_q = [&](const ItemView &w) {
 #pragma unroll
-            for (int r = 0; r < 2; r++) {
+            for (int r = 0; r < kQPer; r++) {
                 const int i = tid + r * kTcSoftmaxWarps * 32, h = i >> 4, c = i & 15;
                 qn[r] = reinterpret_cast<const uint4 *>(a.q_post + (w.hrow + h) * kD)[c];
             }
@@ -501,7 +507,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
         };
         auto store_q = [&]() {
 #pragma unroll
-            for (int r = 0; r < 2; r++) {
+            for (int r = 0; r < kQPer; r++) {
                 const int i = tid + r * kTcSoftmaxWarps * 32, h = i >> 4, c = i & 15;
                 *reinterpret_cast<uint4 *>(sQ + sw128(kTcHeads, h, c)) = qn[r];
             }
@@ -538,7 +544,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                 }
                 tc_fence_after();
                 float y[kTcHalf];
-                tmem_ld16(t_s + sb * 32 + h0 + lane_base, y);
+                tmem_ld(t_s + sb * 32 + h0 + lane_base, y);
                 tc_fence_before();
                 mbar_arrive(B_(bar_sempty[sb]));
                 const int tok = (v.pg0 + 8 * j) * 16 + t;
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                     ok = false;
                     break;
                 }
-                const uint32_t U = (s_any[rb] >> h0) & 0xffffu;
+                const uint32_t U = (s_any[rb] >> h0) & ((1u << kTcHalf) - 1u);
                 // the slot two blocks on was read before everyone arrived here,
                 // and is written again only after everyone arrives next time
                 if (tid < kTcHeads) s_ref[(jg + 2) % 3][tid] = INT_MIN;
@@ -596,10 +602,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
 #pragma unroll
                         for (int part = 0; part < 2; part++) {   // the hi and the lo products
                             float o[kTcHalf];
-                            tmem_ld16(t_o + 32 * part + h0 + lane_base, o);
+                            tmem_ld(t_o + 32 * part + h0 + lane_base, o);
 #pragma unroll
                             for (int h = 0; h < kTcHalf; h++) o[h] *= al[h];
-                            tmem_st16(t_o + 32 * part + h0 + lane_base, o);
+                            tmem_st(t_o + 32 * part + h0 + lane_base, o);
                         }
                     }
                 }
@@ -621,13 +627,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                     ok = false;
                     break;
                 }
-                {   // row t: chunks 0-3 hold P_hi of heads 0-31, chunks 4-7 P_lo
+                {   // row t: chunks 0-3 hold P_hi of heads 0-31 (8 per chunk), chunks 4-7 P_lo
                     uint8_t *row = sP + pb * kTcPBytes + t * 128;
-                    const int c = h0 >> 3;
-                    *reinterpret_cast<uint4 *>(row + ((c ^ (t & 7)) << 4)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                    *reinterpret_cast<uint4 *>(row + (((c + 1) ^ (t & 7)) << 4)) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-                    *reinterpret_cast<uint4 *>(row + (((c + 4) ^ (t & 7)) << 4)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-                    *reinterpret_cast<uint4 *>(row + (((c + 5) ^ (t & 7)) << 4)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+#pragma unroll
+                    for (int q = 0; q < kTcHalf / 8; q++) {
+                        const int c = (h0 >> 3) + q;
+                        *reinterpret_cast<uint4 *>(row + ((c ^ (t & 7)) << 4)) =
+                            make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+                        *reinterpret_cast<uint4 *>(row + (((c + 4) ^ (t & 7)) << 4)) =
+                            make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
+                    }
                 }
                 fence_async_smem();
                 tc_fence_before();
@@ -644,11 +653,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
 #pragma unroll
                 for (int h = 0; h < kTcHalf; h++) s_m[h0 + h] = m[h];
             }
-            // the warp's 32 partial sums of each of its 16 heads: a transposing
-            // butterfly halves the heads a lane holds at each step, so lane
-            // pair (2 i, 2 i + 1) ends with the sum of head i
+            // the warp's 32 partial sums of each of its kTcHalf heads: a
+            // transposing butterfly halves the heads a lane holds at each step,
+            // so lane 2 i (i < kTcHalf) ends with the sum of head i once the
+            // lanes the butterfly did not pair are added
 #pragma unroll
-            for (int w = 8; w >= 1; w >>= 1) {
+            for (int w = kTcHalf / 2; w >= 1; w >>= 1) {
                 const bool upper = (lane & (2 * w)) != 0;
 #pragma unroll
                 for (int i = 0; i < w; i++) {
@@ -658,19 +668,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                 }
             }
             l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
-            if ((lane & 1) == 0) {
-                const int hl = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-                s_l[warp & 3][h0 + hl] = l[0];
-            }
+            if (kTcHalf == 8) l[0] += __shfl_xor_sync(0xffffffffu, l[0], 16);
+            if ((lane & 1) == 0 && lane < 2 * kTcHalf) s_l[warp & 3][h0 + ((lane >> 1) & (kTcHalf - 1))] = l[0];
             mbar_arrive(B_(bar_red));
             if (!mbar_wait_or_fail(B_(bar_red), k & 1, fail)) break;
             if (warp < 4) {   // O^T row tid: the hi and lo products of all 32 heads
                 tc_fence_after();
-                float o[32], o2[32];
-                tmem_ld32(t_o + lane_base, o);
-                tmem_ld32(t_o + 32 + lane_base, o2);
 #pragma unroll
-                for (int h = 0; h < kTcHeads; h++) L.part_o[((size_t)it * L.G + h) * kD + tid] = o[h] + o2[h];
+                for (int c = 0; c < kTcHeads; c += 16) {
+                    float o[16], o2[16];
+                    tmem_ld(t_o + c + lane_base, o);
+                    tmem_ld(t_o + 32 + c + lane_base, o2);
+#pragma unroll
+                    for (int h = 0; h < 16; h++) L.part_o[((size_t)it * L.G + c + h) * kD + tid] = o[h] + o2[h];
+                }
                 if (tid < kTcHeads)
                     L.part_ml[(size_t)it * L.G + tid] =
                         make_float2(s_m[tid], (s_l[0][tid] + s_l[1][tid]) + (s_l[2][tid] + s_l[3][tid]));

@@ -347,3 +347,27 @@ def test_band_holding_the_mass_takes_the_direct_form(amend_band):
     assert st["device_error"] == 0
     # every (request, head) of every step past the band is ill-conditioned
     assert st["removal_direct"] == c.steps * B * H, st["removal_direct"]
+
+
+@pytest.mark.parametrize("kv_heads,context", [(8, 3000), (1, 20000)])
+def test_refused_page_is_reported_and_leaves_other_requests_exact(kv_heads, context):
+    """A page-table entry outside the pool is refused on the device: the step
+    completes, the bounds-check word reports it, and no other request's
+    output moves.  GQA 32/8 runs the mma.sync kernel; MQA at 2 x 20001
+    tokens the tcgen05 kernel."""
+    from gpu_harness import check_out
+    p = _pair(cfg(kv_heads=kv_heads, context=context, steps=1))
+    bad = p.pages[0].clone()
+    bad[5] = 1 << 30
+    p.mac.set_page_table(0, bad.contiguous())
+    dev, host = p.step_inputs(0)
+    ref = p.orc.full_step(host[1], host[2], host[3])
+    out, lse = p.mac.full_step(*dev[1:])
+    torch.cuda.synchronize()
+    st = p.mac.stats()
+    assert st["device_error"] & 1
+    assert st["tcgen05_steps"] == (1 if kv_heads == 1 else 0)
+    check_out(out[1:], lse[1:], {"out": ref["out"][1:], "lse": ref["lse"][1:]}, "request 1")
+    from kv_cache_computation_gb300 import _native as N
+    with pytest.raises(N.MacError):   # the handle reports the refused page and stays failed
+        p.mac.sync()
