@@ -4,25 +4,28 @@
 // paper; the plan is the span-proportional one of Figure 3(b), made in every
 // CTA's prologue as in the mma.sync kernel).
 //
-// One CTA per SM.  The KV stream is cut into blocks of 128 tokens (8 pages);
-// a block's keys and its values go through rings of their own in shared
-// memory (kTcKStages and kTcVStages blocks), each stage filled by a warp of
-// its own with cp.async in the 128-byte swizzled layout the tensor core
-// reads: rows of 128 bytes, the 16-byte chunk c of row t at c ^ (t mod 8), a
-// 64-element column block per 16 KB.  Tokens are the M of both products and
-// the group's 32 heads their N, so no work is spent on padding:
+// One CTA of 11 warps per SM, for steps of at least 32768 KV tokens (the host
+// picks this kernel or the mma.sync one per step).  The KV stream is cut into
+// blocks of 128 tokens (8 pages); a block's keys and its values go through
+// rings of their own in shared memory (kTcKStages and kTcVStages blocks), each
+// filled by TMA from a loader warp of its own (two 16-row x 64-column boxes per
+// page) in the 128-byte swizzled layout the tensor core reads: rows of 128
+// bytes, the 16-byte chunk c of row t at c ^ (t mod 8), a 64-element column
+// block per 16 KB.  Tokens are the M of both products and the group's 32 heads
+// their N, so no work is spent on padding:
 //   S^T[128 x 32]  = K[128 x 128] Q^T                 (8 mma, M 128, N 32, K 16)
 //   O^T[128 x 64] += V^T[128 x 128] [P_hi P_lo]^T      (8 mma, M 128, N 64; V is
 //                                                     read MN-major)
-// Thread t of the four softmax warps owns token row t of S^T (TMEM lane t):
-// the block's 32 scores of its token.  All threads keep one softmax reference
-// per head, which moves only when a block passes it by more than 2^8; the
-// threads agree on the moves of a block through shared memory and a bounded
-// mbarrier, and a move rescales O^T in tensor memory (thread d holds row d:
-// head h in columns h and 32 + h).  P is kept as a bf16 pair (hi, lo) per
-// head, so the product P V keeps about 16 bits of P.  Each thread sums its own
-// token's P per head; the 128 partial sums of a head are added when the item
-// ends.
+// issued by one thread of a warp of its own.  Softmax thread (t, w / 4) of
+// warp w owns token row t of S^T (TMEM lane t) for kTcHalf heads.  All threads
+// keep one softmax reference per head, which moves only when a block passes it
+// by more than 2^8; the threads agree on the moves of a block through shared
+// memory and a bounded mbarrier, and a move rescales O^T in tensor memory
+// (thread d holds row d: head h in columns h and 32 + h).  P is kept as a bf16
+// pair (hi, lo) per head, so the product P V keeps about 16 bits of P.  Each
+// thread sums its own token's P per head; the 128 partial sums of a head are
+// added when the item ends.  The roles walk the CTA's items independently, so
+// the next item's copies and score products overlap the current item's merge.
 //
 // Every wait on an mbarrier has an iteration limit; on expiry the kernel sets
 // kErrTimeout, lets its copies land, frees its tensor memory and returns.
@@ -206,15 +209,17 @@ __device__ __forceinline__ int ord_key(float f)
 }
 __device__ __forceinline__ float ord_val(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
 
-// Roles: warps 0-7 softmax (warp w: TMEM lanes 32 (w mod 4) .. + 31, i.e.
-// token rows of S^T and rows of O^T, for heads 16 (w / 4) .. + 15), warp
-// kTcKWarp / kTcVWarp loads the key / value blocks by TMA, warp kTcMmaWarp
-// issues the tensor-core work.  Barriers: kfull / vfull (a stage's bytes
-// landed), kempty / vempty (the block's score / P V product done), sfull /
-// sempty and pfull / pempty per S^T and P buffer, mv (the softmax threads'
-// agreement on a block's moves).  Completion k of a barrier is awaited with
-// parity k & 1; every role waits each completion in order, so no barrier
-// runs two phases ahead of a waiter.
+// Roles: warps 0 .. kTcSoftmaxWarps - 1 softmax (warp w: TMEM lanes
+// 32 (w mod 4) .. + 31, i.e. token rows of S^T and rows of O^T, for heads
+// kTcHalf (w / 4) .. + kTcHalf - 1), warp kTcKWarp / kTcVWarp loads the key /
+// value blocks by TMA, warp kTcMmaWarp issues the tensor-core work.  Barriers:
+// kfull / vfull (a stage's bytes landed), kempty / vempty (the block's score /
+// P V product done), sfull / sempty and pfull / pempty per S^T and P buffer,
+// mv (the softmax threads' agreement on a block's moves), qfull (an item's Q
+// stored), red (the merge's partial sums stored), oempty (O^T read by the
+// merge), done (every product issued complete).  Completion k of a barrier is
+// awaited with parity k & 1; every role waits each completion in order, so no
+// barrier runs two phases ahead of a waiter.
 template <int KS, int VS>
 __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __grid_constant__ Layout L, StepArgs a, const __grid_constant__ TcMaps M)
 {
@@ -487,8 +492,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
             mbar_wait_bounded(B_(bar_done), 0);
         }
     } else {
-        // softmax: thread (t, half) holds token t of each block for the heads
-        // h0 .. h0 + 15
+        // softmax: thread (t, w / 4) holds token t of each block for the heads
+        // h0 .. h0 + kTcHalf - 1
         const int t = tid & (kTcTok - 1), h0 = (warp >> 2) * kTcHalf;
         // Q of an item (thread: chunks tid, tid + 32 x kTcSoftmaxWarps, ... of
         // the 32 x 16) and its heads' first tokens, fetched one item ahead into
