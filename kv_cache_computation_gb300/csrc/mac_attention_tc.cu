@@ -567,11 +567,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                     if (y[h] - m[h] > kLazyMax) mv |= 1u << h;
                 const uint32_t wmv = __reduce_or_sync(0xffffffffu, mv);
                 if (wmv) {
+                    if (__popc(wmv) > 2) {
+                        // many heads moved (an item's first block): the warp's
+                        // maxima by a transposing butterfly, lane 2 i ending
+                        // with head i's, then one shared atomic per head
+                        int kk[kTcHalf];
 #pragma unroll
-                    for (int h = 0; h < kTcHalf; h++) {
-                        if (wmv >> h & 1u) {
-                            const int key = __reduce_max_sync(0xffffffffu, (mv >> h & 1u) ? ord_key(y[h]) : INT_MIN);
-                            if (lane == 0) atomicMax(&s_ref[rb][h0 + h], key);
+                        for (int h = 0; h < kTcHalf; h++) kk[h] = (mv >> h & 1u) ? ord_key(y[h]) : INT_MIN;
+#pragma unroll
+                        for (int w = kTcHalf / 2; w >= 1; w >>= 1) {
+                            const bool upper = (lane & (2 * w)) != 0;
+#pragma unroll
+                            for (int i = 0; i < w; i++) {
+                                const int send = upper ? kk[i] : kk[w + i];
+                                const int keep = upper ? kk[w + i] : kk[i];
+                                kk[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, 2 * w));
+                            }
+                        }
+                        kk[0] = max(kk[0], __shfl_xor_sync(0xffffffffu, kk[0], 1));
+                        if (kTcHalf == 8) kk[0] = max(kk[0], __shfl_xor_sync(0xffffffffu, kk[0], 16));
+                        const int hl = (lane >> 1) & (kTcHalf - 1);
+                        if ((lane & 1) == 0 && lane < 2 * kTcHalf && (wmv >> hl & 1u)) atomicMax(&s_ref[rb][h0 + hl], kk[0]);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < kTcHalf; h++) {
+                            if (wmv >> h & 1u) {
+                                const int key = __reduce_max_sync(0xffffffffu, (mv >> h & 1u) ? ord_key(y[h]) : INT_MIN);
+                                if (lane == 0) atomicMax(&s_ref[rb][h0 + h], key);
+                            }
                         }
                     }
                     if (lane == 0) atomicOr(&s_any[rb], wmv << h0);
@@ -654,6 +677,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
             // merge: the item's last P V done, O^T holds the hi and lo products
             const uint32_t last = jbase + v.nblk - 1;
             if (!mbar_wait_or_fail(B_(bar_pempty[last & 1]), (last >> 1) & 1, fail)) break;
+            {   // O^T row t for this thread's heads (hi + lo), then O^T is free for the next item
+                tc_fence_after();
+                float o[kTcHalf], o2[kTcHalf];
+                tmem_ld(t_o + h0 + lane_base, o);
+                tmem_ld(t_o + 32 + h0 + lane_base, o2);
+                tc_fence_before();
+                mbar_arrive(B_(bar_oempty));
+#pragma unroll
+                for (int h = 0; h < kTcHalf; h++) L.part_o[((size_t)it * L.G + h0 + h) * kD + t] = o[h] + o2[h];
+            }
             if (t == 0) {
 #pragma unroll
                 for (int h = 0; h < kTcHalf; h++) s_m[h0 + h] = m[h];
@@ -677,22 +710,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
             if ((lane & 1) == 0 && lane < 2 * kTcHalf) s_l[warp & 3][h0 + ((lane >> 1) & (kTcHalf - 1))] = l[0];
             mbar_arrive(B_(bar_red));
             if (!mbar_wait_or_fail(B_(bar_red), k & 1, fail)) break;
-            if (warp < 4) {   // O^T row tid: the hi and lo products of all 32 heads
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < kTcHeads; c += 16) {
-                    float o[16], o2[16];
-                    tmem_ld(t_o + c + lane_base, o);
-                    tmem_ld(t_o + 32 + c + lane_base, o2);
-#pragma unroll
-                    for (int h = 0; h < 16; h++) L.part_o[((size_t)it * L.G + c + h) * kD + tid] = o[h] + o2[h];
-                }
-                if (tid < kTcHeads)
-                    L.part_ml[(size_t)it * L.G + tid] =
-                        make_float2(s_m[tid], (s_l[0][tid] + s_l[1][tid]) + (s_l[2][tid] + s_l[3][tid]));
-            }
-            tc_fence_before();
-            mbar_arrive(B_(bar_oempty));
+            if (tid < kTcHeads)
+                L.part_ml[(size_t)it * L.G + tid] =
+                    make_float2(s_m[tid], (s_l[0][tid] + s_l[1][tid]) + (s_l[2][tid] + s_l[3][tid]));
             jbase += v.nblk;
         }
     }
