@@ -116,7 +116,7 @@ typedef struct {
     uint32_t reserved;
     uint64_t tcgen05_steps;   /* of the steps, those whose attention ran on the */
                               /* tcgen05 kernel (groups of 32 heads, steps of   */
-                              /* at least 32768 KV tokens); the others ran on   */
+                              /* at least 16384 KV tokens); the others ran on   */
                               /* the mma.sync kernel                            */
 } mac_stats;
 

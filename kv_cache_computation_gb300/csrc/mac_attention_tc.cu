@@ -4,7 +4,7 @@
 // paper; the plan is the span-proportional one of Figure 3(b), made in every
 // CTA's prologue as in the mma.sync kernel).
 //
-// One CTA of 11 warps per SM, for steps of at least 32768 KV tokens (the host
+// One CTA of 11 warps per SM, for steps of at least 16384 KV tokens (the host
 // picks this kernel or the mma.sync one per step).  The KV stream is cut into
 // blocks of 128 tokens (8 pages); a block's keys and its values go through
 // rings of their own in shared memory (kTcKStages and kTcVStages blocks), each

@@ -93,7 +93,7 @@ constexpr int kHmWideGroups = MAC_HM_WIDE_GROUPS;
 #define MAC_ATTN_TC32 1
 #endif
 #ifndef MAC_TC_MIN_TOKENS
-#define MAC_TC_MIN_TOKENS 32768
+#define MAC_TC_MIN_TOKENS 16384
 #endif
 constexpr long long kTcMinTokens = MAC_TC_MIN_TOKENS;
 // Steps of at least MAC_TC_WAVE_TOKENS KV tokens per tcgen05 CTA are planned

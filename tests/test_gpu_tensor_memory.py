@@ -1,7 +1,7 @@
 """GPU parity of the tcgen05 attention kernel against the fp64 oracle.
 
 Groups of 32 query heads (MQA-shaped GQA) go through the tcgen05 kernel in
-steps that hold at least 32768 KV tokens over all requests and KV heads;
+steps that hold at least 16384 KV tokens over all requests and KV heads;
 smaller steps keep the mma.sync kernel.  These cases are sized to land on
 either side of that line (the handle reports which kernel ran), with ragged
 request lengths, several 128-token blocks per work item, items that start
@@ -70,3 +70,17 @@ def test_small_steps_of_32_head_groups_keep_the_mma_sync_kernel():
     st = p.mac.stats()
     assert st["device_error"] == 0
     assert st["tcgen05_steps"] == 0
+
+
+@pytest.mark.parametrize("amend_band", [0, 1])
+def test_one_request_just_past_the_line(amend_band):
+    # one MQA request of 17 000 tokens: the single group is cut into items of
+    # about one 128-token block each, most starting and ending inside a block
+    c = cfg(batch=1, context=17000, steps=4)
+    p = _pair(c, amend_band=amend_band)
+    p.full_step(0)
+    for t in range(1, 4):
+        p.mac_step(t, force=True)
+    st = p.mac.stats()
+    assert st["device_error"] == 0
+    assert st["tcgen05_steps"] == 4
