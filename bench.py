@@ -383,6 +383,8 @@ def method_points(dev, peak, specs, steps=48, warm=4, prof_steps=16, eager=False
             phases = {k.replace("_ms", ""): round(pr[k] * 1e3 / n_p, 2)
                       for k in ("match_plan_ms", "attention_ms", "combine_ms")}
             phases["work_items"] = round(st_p["work_items"] / n_p, 1)
+            # the attention kernel the step ran on (the library picks it per step)
+            phases["kernel"] = "tcgen05" if st_p.get("tcgen05_steps", 0) > 0 else "mma.sync"
             return us, st, kv_read, kv_full, attn_us, attn_gbs, phases
 
         for rate in rates:
