@@ -386,9 +386,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                     break;
                 }
                 const uint32_t have = __ballot_sync(0xffffffffu, lane < 8 && row >= 0);
-                int rows[8];
-#pragma unroll
-                for (int p = 0; p < 8; p++) rows[p] = __shfl_sync(0xffffffffu, row, p);
                 if (have != 0xffu) {
                     // a page past the item or refused by the table is not copied:
                     // its rows are zeroed (the generic writes fenced for the
@@ -403,16 +400,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                     fence_async_smem();
                     __syncwarp();
                 }
-                if (lane == 0) {
+                {   // lane 0 arms the stage's byte count, then lane 2 p + h copies half h of page p
                     const uint32_t f = B_(full[st]);
-                    mbar_expect_tx(f, (uint32_t)__popc(have) * 2u * 2048u);
-                    const uint32_t d0 = ring + st * kTcBlockBytes;
-#pragma unroll
-                    for (int p = 0; p < 8; p++) {
-                        if (rows[p] < 0) continue;
-                        tma_load_2d(d0 + p * 2048, map, 0, rows[p], f);
-                        tma_load_2d(d0 + kTcTok * 128 + p * 2048, map, 64, rows[p], f);
-                    }
+                    if (lane == 0) mbar_expect_tx(f, (uint32_t)__popc(have) * 2u * 2048u);
+                    __syncwarp();
+                    const int hf = lane & 1, rp = __shfl_sync(0xffffffffu, row, (lane >> 1) & 7);
+                    if (lane < 16 && rp >= 0)
+                        tma_load_2d(ring + st * kTcBlockBytes + hf * (kTcTok * 128) + (lane >> 1) * 2048, map, hf * 64, rp, f);
                 }
                 issued++;
             }
