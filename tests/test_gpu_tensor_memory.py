@@ -84,3 +84,39 @@ def test_one_request_just_past_the_line(amend_band):
     st = p.mac.stats()
     assert st["device_error"] == 0
     assert st["tcgen05_steps"] == 4
+
+
+@pytest.mark.parametrize("amend_band", [0, 1])
+def test_graph_captured_loop_on_the_tensor_memory_kernel(amend_band):
+    """MQA steps of 2 x 9001+ tokens captured into a CUDA graph (programmatic
+    dependent launches between the step's kernels) and replayed: every
+    replayed step equals the oracle's, the GPU making its own decisions."""
+    import oracle
+    from gpu_harness import check_out, KEYS
+    c = cfg(batch=2, context=9000, steps=11)
+    p = _pair(c, amend_band=amend_band)
+    for t in range(2):                           # eager steps first
+        p.mac_step(t, force=False, check_ring=False)
+    assert p.mac.stats()["tcgen05_steps"] == 2
+    p.mac.sync()
+    B, H = c.batch, c.heads
+    ins = [[p.inputs[k][t].cuda().contiguous() for k in KEYS] for t in range(2, 10)]
+    outs = [torch.empty((B, H, 128), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    lses = [torch.empty((B, H), dtype=torch.float32, device="cuda") for _ in range(8)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(8):
+                p.mac.decode_step(*ins[i], out=outs[i], lse=lses[i])
+            p.mac.join()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(8):
+        ref = p.orc.step(*[W.bf16_bits(p.inputs[k][i + 2]) for k in KEYS])
+        assert not oracle.decision_flags(ref["D"], ref["D2"], ref["qn2"], c.tau).any()
+        check_out(outs[i], lses[i], ref, f"graph step {i}")
+    p.check_ring(9)
+    assert p.mac.stats()["device_error"] == 0
