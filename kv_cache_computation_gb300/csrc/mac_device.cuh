@@ -171,7 +171,14 @@ __device__ __forceinline__ ChunkDiv chunk_div(int C)
 {
     const unsigned c = (unsigned)C >> 4;
     const int k = 26 + (32 - __clz(c - 1));
-    return {(unsigned)(((1ull << k) + c - 1) / c), k};
+    // m = ceil(2^k / c), below 2^27: a float quotient (within 2 ulp, i.e. 32,
+    // of the exact one) corrected by integer steps -- no 64-bit division,
+    // which costs about a thousand cycles in the plan's critical path
+    const unsigned long long p2 = 1ull << k;
+    unsigned long long m = (unsigned long long)__fdividef(__int_as_float((127 + k) << 23), (float)c);
+    while (m * c < p2) m++;
+    while ((m - 1) * c >= p2) m--;
+    return {(unsigned)m, k};
 }
 
 __device__ __forceinline__ int div_c(int x, ChunkDiv d)

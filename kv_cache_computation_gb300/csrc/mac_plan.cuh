@@ -24,7 +24,8 @@ namespace {
 // most C tokens, so the step finishes when the longest item does; the plan
 // takes the smallest C for which the long items fit one wave of the
 // persistent attention grid (or k waves when there are more long segments
-// than CTAs).  The short band items either come on top -- a CTA that takes
+// than CTAs), searched by bisection (aligned chunk counts are not strictly
+// monotone in C, so it may settle on a slightly larger C that also fits).  The short band items either come on top -- a CTA that takes
 // one starts its long item that much later, which idle CTAs or the page
 // pools below absorb -- or are fitted into the wave, which lengthens every
 // long item by about nb / (P - nb); band_wave_fit picks the cheaper.
@@ -67,9 +68,11 @@ __device__ __forceinline__ int plan_chunk(const Layout &L, const StepArgs &a, co
     return max(kMinChunk, round_up16(((long long)(hi - lo) + splits - 1) / splits));
 }
 
-// Up to 32 groups: one warp plans alone -- lane g holds group g, 32 chunk
-// candidates are counted at once (lane k counts candidate k), a ballot picks
-// the smallest that fits, a shuffle scan gives the offsets.
+// Up to 32 groups: one warp plans alone -- lane g holds group g; up to 8
+// groups, 32 chunk candidates are counted at once (lane k counts candidate
+// k), a ballot picks the smallest that fits; above that the chunk is found by
+// bisection (each probe one warp sum of the groups' chunk counts); a shuffle
+// scan gives the offsets.
 __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &ps)
 {
     const int nbg = a.batch * L.Hkv;
@@ -101,41 +104,59 @@ __device__ bool cta_plan_small(const Layout &L, const StepArgs &a, PlanShared &p
         int Q = (4 * nseg <= P) ? P : P * (1 + (2 * nseg + P - 1) / P);
         if (Q == P && band_wave_fit(nb, TL, P, L.band_r)) Q = P - nb;
         if (Q > L.item_cap - nb) Q = L.item_cap - nb;
-        // The smallest fitting chunk is at least T / Q (count(C) >= T / C)
-        // and at most T / (Q - 2 nseg) (count(C) < T / C + 2 nseg).  Float
-        // quotients (relative error < 2^-22) widened by 2^-20 bracket both.
+        // A fitting chunk is at least T / Q (count(C) >= T / C), and
+        // T / (Q - 2 nseg) fits (count(C) < T / C + 2 nseg).  Float quotients
+        // (relative error < 2^-22) widened by 2^-20 bracket both.
         const float Tq = (float)TL;
         long long c_lo = (long long)(Tq / (float)Q * (1.f - 0x1p-20f)) / 16 * 16;
         long long c_hi = Q > 2 * nseg ? round_up16((long long)(Tq / (float)(Q - 2 * nseg) * (1.f + 0x1p-20f)) + 16)
                                       : (1ll << 30);
         if (c_lo < kMinChunk) c_lo = kMinChunk;
         if (c_hi < c_lo) c_hi = c_lo;
-        // candidates c_lo + 16 * stride * k, k = 0..31 (the last one is c_hi)
-        for (;;) {
-            const long long span16 = (c_hi - c_lo) / 16;
-            const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
-            long long cand = c_lo + 16 * stride * lane;
-            if (cand > c_hi) cand = c_hi;
-            const ChunkDiv R = chunk_div((int)cand);
-            int cnt = 0;
+        if (nbg <= 8) {
+            // few groups: lane k counts candidate c_lo + 16 * stride * k
+            // (k = 0..31, the last one c_hi) over every group, a ballot picks
+            // the smallest that fits
+            for (;;) {
+                const long long span16 = (c_hi - c_lo) / 16;
+                const long long stride = span16 <= 31 ? 1 : (span16 + 30) / 31;
+                long long cand = c_lo + 16 * stride * lane;
+                if (cand > c_hi) cand = c_hi;
+                const ChunkDiv R = chunk_div((int)cand);
+                int cnt = 0;
 #pragma unroll 4
-            for (int g = 0; g < nbg; g++) {
-                const int glo = ps.lo[g], ghi = ps.hi[g], gsp = plan_split(L, a, glo, ghi);
-                cnt += n_chunks_c(glo, gsp, R);
+                for (int g = 0; g < nbg; g++) {
+                    const int glo = ps.lo[g], ghi = ps.hi[g], gsp = plan_split(L, a, glo, ghi);
+                    cnt += n_chunks_c(glo, gsp, R);
+                }
+                const unsigned fit = __ballot_sync(0xffffffffu, cnt <= Q);
+                const int k = fit ? __ffs(fit) - 1 : 31;
+                const long long ck = __shfl_sync(0xffffffffu, cand, k);
+                if (stride == 1 || k == 0) {
+                    c_hi = ck;
+                    RC.m = __shfl_sync(0xffffffffu, R.m, k);
+                    RC.k = __shfl_sync(0xffffffffu, R.k, k);
+                    break;
+                }
+                c_hi = ck;   // refine between the previous candidate and this one
+                c_lo = __shfl_sync(0xffffffffu, cand, k - 1) + 16;
             }
-            const unsigned fit = __ballot_sync(0xffffffffu, cnt <= Q);
-            const int k = fit ? __ffs(fit) - 1 : 31;
-            const long long ck = __shfl_sync(0xffffffffu, cand, k);
-            if (stride == 1 || k == 0) {
-                c_hi = ck;
-                RC.m = __shfl_sync(0xffffffffu, R.m, k);
-                RC.k = __shfl_sync(0xffffffffu, R.k, k);
-                break;
+            C = (int)c_hi;
+        } else {
+            // binary search over the multiples of 16 in [c_lo, c_hi], lane g
+            // counting group g's chunks (one warp sum per probe): c_hi fits, and
+            // the search only ever moves its upper end to a chunk that fits
+            int lo16 = (int)(c_lo >> 4), hi16 = (int)(c_hi >> 4);
+            while (lo16 < hi16) {
+                const int mid = (lo16 + hi16) >> 1;
+                const ChunkDiv R = chunk_div(mid << 4);
+                const int cnt = warp_sum_int(lane < nbg ? n_chunks_c(lo, sp, R) : 0);
+                if (cnt <= Q) hi16 = mid;
+                else lo16 = mid + 1;
             }
-            c_hi = ck;   // refine between the previous candidate and this one
-            c_lo = __shfl_sync(0xffffffffu, cand, k - 1) + 16;
+            C = hi16 << 4;
+            RC = chunk_div(C);
         }
-        C = (int)c_hi;
     }
     // per-group counts and offsets
     int cnt = 0;

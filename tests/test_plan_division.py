@@ -41,3 +41,34 @@ def test_multiplier_division_is_exact():
                     xs.add(v)
         for x in xs:
             assert div_c(x, d) == x // C, (x, C)
+
+
+def _chunk_div_device_steps(C, ulp_off):
+    """The kernel's steps for m: a float quotient 2^k / c (perturbed by
+    ulp_off units in the last place, the fast division's error bound is 2),
+    then +1 / -1 steps to the smallest m with m c >= 2^k."""
+    c = C >> 4
+    k = 26 + (c - 1).bit_length()
+    q = np.float32(np.float32(2.0 ** k) / np.float32(c))
+    for _ in range(abs(ulp_off)):
+        q = np.nextafter(q, np.float32(np.inf) if ulp_off > 0 else np.float32(0), dtype=np.float32)
+    m = int(q)
+    steps = 0
+    while m * c < (1 << k):
+        m += 1
+        steps += 1
+    while (m - 1) * c >= (1 << k):
+        m -= 1
+        steps += 1
+    return m, k, steps
+
+
+def test_device_multiplier_steps_reach_the_exact_multiplier():
+    rng = np.random.default_rng(20261202)
+    cs = sorted(set([4, 5, 7, 8, 9, 31, 32, 33, 1 << 20, (1 << 25) + 3, (1 << 26) - 1, 1 << 26]
+                    + rng.integers(4, 1 << 26, 2000).tolist() + list(range(4, 600))))
+    for c in cs:
+        for off in (-2, 0, 2):
+            m, k, steps = _chunk_div_device_steps(int(c) * 16, off)
+            assert (m, k) == chunk_div(int(c) * 16), (c, off)
+            assert steps <= 40, (c, off, steps)
