@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
 
     if (warp == kTcKWarp || warp == kTcVWarp) {
         // block j of an item goes to stage (jbase + j) mod KS (VS) of the
-        // ring; lanes 0-7 look up the pages of the blocks two ahead, lane 0
-        // issues the copies: per page, its two 64-column halves
+        // ring; lanes 0-7 look up the pages of the blocks two ahead, lanes
+        // 0-15 issue the copies: per page, its two 64-column halves
         const bool keys = warp == kTcKWarp;
         const int ns = keys ? KS : VS;
         uint64_t *full = keys ? bar_kfull : bar_vfull;
