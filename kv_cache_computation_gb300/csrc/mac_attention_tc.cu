@@ -134,7 +134,7 @@ __device__ __forceinline__ void mbar_wait_bounded(uint32_t mbar, uint32_t parity
 
 // Bounded wait that also gives up once another role has failed.  The lanes
 // of a warp run it in step on the same barrier word and the same flag, so
-// they leave it together with the same verdict before any warp-wide
+// they leave it together with the same outcome before any warp-wide
 // instruction that follows.
 __device__ __forceinline__ bool mbar_wait_or_fail(uint32_t mbar, uint32_t parity, volatile int *fail)
 {
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attention_tc_kernel(const __gri
                 const int row = resolve(e0);
                 e0 = e1;
                 e1 = fetch(j + 2);
-                bool go = true;   // lane 0 waits for the stage, the warp follows its verdict
+                bool go = true;   // lane 0 waits for the stage, the warp follows its outcome
                 if (lane == 0 && round >= 1) go = mbar_wait_or_fail(B_(empty[st]), (round - 1) & 1, fail);
                 if (!__shfl_sync(0xffffffffu, go, 0)) {
                     ok = false;

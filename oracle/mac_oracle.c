@@ -158,7 +158,7 @@ double orc_log1mexp(double x)
 /* via online subtraction"): given the summary of A u B and of B, recover A. */
 /*   delta = lB - lAuB (<= 0),  lA = lAuB + log(1 - e^delta),                */
 /*   oA = (oAuB - e^delta oB) / (1 - e^delta).                               */
-/* Returns the conditioning 1 - e^delta so the caller can judge it (R7).     */
+/* Returns the conditioning 1 - e^delta so the caller can test it (R7).      */
 /* ------------------------------------------------------------------------ */
 double orc_remove(const double *oab, double lab, const double *ob, double lb, int d,
                   double *o, double *l)
